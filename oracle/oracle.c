@@ -1,0 +1,566 @@
+/*
+ * oracle.c -- reference definition of batched speculative verification and of
+ * the confidence-scheduled verify-length selector, written as plain,
+ * single-threaded fp64 C.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  It shares no code,
+ * header, constant table or helper with the CUDA path, and it is never on the
+ * product path.
+ *
+ * Sources (pages on speculative decoding):
+ *   [AS]  "AngelSpec: Towards Real-World High Performance Inference with
+ *         Speculative Decoding" -- §2.3 eqs. (4)-(5) (TV distance, overlap);
+ *         §4.1 (keep depths n_i, budget K = sum (n_i + 1)); §4.2 eqs. (19)-(24)
+ *         (prefix survival, estimated progress, top-K with shallow-first ties,
+ *         budget selection against a profiled cost).
+ *   [BL]  "breaking down dspark and its lineage" (blog) -- section
+ *         "Preserving the target distribution during verification" (accept if
+ *         p(x) >= q(x), else with probability p(x)/q(x); on rejection resample
+ *         from the normalised residual max(p - q, 0)); section "Verify smarter,
+ *         not longer" (prefix scheduler in prose).
+ *   [US]  "UraionSpec: A Faithful Implementation of Confidence-Scheduled
+ *         Speculative Decoding" -- §2.1 eq. (acceptance) and eq. (expected_tau);
+ *         §3.5 Algorithm 1 (hardware-aware prefix scheduler).
+ *
+ * Readings taken where the pages are silent (each is also listed in the design
+ * notes):
+ *   - Temperature: p = softmax(z / T).  T == 0 is greedy: accept while the
+ *     draft token equals the target argmax; the emitted token is the target
+ *     argmax of the first rejected row (or of row ell_b).  Argmax ties go to
+ *     the lowest index.
+ *   - Accept test written without division: accept iff u * q(x) < p(x), which
+ *     equals u < min(1, p(x)/q(x)) for u in [0, 1).
+ *   - Uniform slots per request: [0, gamma) accept tests by position, gamma
+ *     the residual draw, gamma + 1 the bonus draw.
+ *   - Residual on rejection at n < ell_b; bonus from p of target row ell_b when
+ *     every tested draft is accepted ([BL], [AS] §1); ell_b = 0 is a pure draw
+ *     from p of target row 0.
+ *   - Draw by inverse CDF: the smallest v with cumsum_{i<=v} w_i > u * sum(w),
+ *     cumsum left to right in fp64.  If the residual sums to zero in floating
+ *     point, draw from p of the same row instead.  If rounding leaves no v, take
+ *     the last v with positive weight.
+ *   - A needed row whose max is not finite (a NaN, +inf, or all -inf) makes the
+ *     request invalid, as do a draft token outside [0, V) at a tested position,
+ *     a uniform outside [0, 1) in a used slot, or ell_b outside [0, gamma].
+ *     Invalid requests emit accept_len -1 and tokens -1.
+ *   - Scheduler budget N = sum_b (ell_b + 1) (bonus positions count) and the
+ *     objective is tau(N) / C(N), C a piecewise-linear cost table.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* Per-request status values (same numbers as the library's error codes). */
+#define OR_OK 0
+#define OR_ERR_SHAPE -2
+#define OR_ERR_TEMPERATURE -4
+#define OR_ERR_VERIFY_LEN -5
+#define OR_ERR_TOKEN -6
+#define OR_ERR_COST_TABLE -8
+#define OR_ERR_NONFINITE -9
+#define OR_ERR_UNIFORM -12
+#define OR_ERR_CONFIDENCE -13
+
+/* event bits reported per request */
+#define EV_RESIDUAL_EMPTY 1 /* residual summed to zero: drew from p instead */
+#define EV_NO_BIN 2         /* rounding left no bin above u*W: took last positive */
+
+/* ------------------------------------------------------------------ inputs */
+
+/* Widen one stored logit to fp64.  dtype 0 = fp32, 1 = bf16 (upper half of an
+ * fp32 bit pattern), both exact. */
+static double logit_at(const void* base, int dtype, int64_t idx) {
+    if (dtype == 0) return (double)((const float*)base)[idx];
+    uint32_t bits = (uint32_t)((const uint16_t*)base)[idx] << 16;
+    float f;
+    memcpy(&f, &bits, 4);
+    return (double)f;
+}
+
+/* ------------------------------------------------- softmax of one row (T>0)
+ * p_v = exp(y_v - m) / sum_u exp(y_u - m), y = z / T, m = max y.
+ * The temperature-scaled softmax the acceptance rule is stated on
+ * ([US] §2.1 eq. (acceptance); [AS] §2.5 names T = 0 and T = 0.9 settings).
+ * Returns OR_ERR_NONFINITE when the row max is not finite. */
+static int row_softmax(const void* base, int dtype, int64_t off, int V, double T, double* p) {
+    double m = -INFINITY;
+    for (int v = 0; v < V; ++v) {
+        double y = logit_at(base, dtype, off + v) / T;
+        if (isnan(y)) return OR_ERR_NONFINITE;
+        p[v] = y;
+        if (y > m) m = y;
+    }
+    if (!isfinite(m)) return OR_ERR_NONFINITE;
+    double S = 0.0;
+    for (int v = 0; v < V; ++v) {
+        p[v] = exp(p[v] - m);
+        S += p[v];
+    }
+    for (int v = 0; v < V; ++v) p[v] = p[v] / S;
+    return OR_OK;
+}
+
+/* Greedy row: argmax of z with the lowest index on ties. */
+static int row_argmax(const void* base, int dtype, int64_t off, int V, int32_t* arg) {
+    double m = -INFINITY;
+    int32_t a = 0;
+    int have = 0;
+    for (int v = 0; v < V; ++v) {
+        double z = logit_at(base, dtype, off + v);
+        if (isnan(z)) return OR_ERR_NONFINITE;
+        if (!have || z > m) { m = z; a = v; have = 1; }
+    }
+    if (!isfinite(m)) return OR_ERR_NONFINITE;
+    *arg = a;
+    return OR_OK;
+}
+
+/* Inverse-CDF draw over nonnegative weights w[0..V-1]:
+ * the smallest v with (w_0 + ... + w_v) > u * W, W the left-to-right sum.
+ * Writes the normalised CDF edges of the chosen bin to *lo, *hi. */
+static int32_t inverse_cdf(const double* w, int V, double u, double* lo, double* hi, int* ev) {
+    double W = 0.0;
+    for (int v = 0; v < V; ++v) W += w[v];
+    double target = u * W;
+    double cum = 0.0;
+    for (int v = 0; v < V; ++v) {
+        double before = cum;
+        cum += w[v];
+        if (cum > target) {
+            *lo = before / W;
+            *hi = cum / W;
+            return v;
+        }
+    }
+    /* rounding left no bin: the last bin with positive weight */
+    *ev |= EV_NO_BIN;
+    cum = 0.0;
+    int32_t last = V - 1;
+    double lo_last = 0.0, hi_last = 1.0;
+    for (int v = 0; v < V; ++v) {
+        double before = cum;
+        cum += w[v];
+        if (w[v] > 0.0) { last = v; lo_last = before / W; hi_last = cum / W; }
+    }
+    *lo = lo_last;
+    *hi = hi_last;
+    return last;
+}
+
+static int uniform_ok(float u) { return u >= 0.0f && u < 1.0f; }
+
+/* -------------------------------------------------------------- verification
+ * Batched lossless verification, one request at a time.
+ *
+ * Layouts (row-major, contiguous):
+ *   target   [B, gamma+1, V]  dtype 0 fp32 / 1 bf16
+ *   draft    [B, gamma,   V]  (not read when T == 0)
+ *   tokens   [B, gamma] int32, verify_len [B] int32 (NULL -> gamma)
+ *   uniforms [B, gamma+2] fp32 (not read when T == 0)
+ * Outputs: out_tokens [B, gamma+1] (-1 after the emitted token),
+ *          out_accept_len [B] (-1 for an invalid request).
+ * Diagnostics (each may be NULL):
+ *   px, qx      [B, gamma]  p(x_j), q(x_j) for j < ell_b (NaN elsewhere / T == 0)
+ *   margin      [B, gamma]  |u_j - p(x_j)/q(x_j)| at every tested position j
+ *   resid_mass  [B]         sum of the draw's weights (residual or p)
+ *   cdf_lo/hi   [B]         normalised CDF edges of the drawn bin
+ *   u_draw      [B]         the uniform the draw used
+ *   status      [B]         per-request status
+ *   events      [B]         EV_* bits
+ * Returns OR_OK, or a shape / temperature error for the whole call. */
+int oracle_verify(const void* target, const void* draft, int dtype, int B, int gamma, int V,
+                  const int32_t* tokens, const int32_t* verify_len, double T,
+                  const float* uniforms, int32_t* out_tokens, int32_t* out_accept_len,
+                  double* px, double* qx, double* margin, double* resid_mass, double* cdf_lo,
+                  double* cdf_hi, double* u_draw, int32_t* status, int32_t* events) {
+    if (B < 0 || gamma < 0 || gamma > 63 || V < 1 || (dtype != 0 && dtype != 1)) return OR_ERR_SHAPE;
+    if (!(T >= 0.0) || !isfinite(T)) return OR_ERR_TEMPERATURE;
+    const int G1 = gamma + 1, G2 = gamma + 2;
+    double* p = (double*)malloc(sizeof(double) * (size_t)V);
+    double* q = (double*)malloc(sizeof(double) * (size_t)V);
+    double* w = (double*)malloc(sizeof(double) * (size_t)V);
+    if (!p || !q || !w) { free(p); free(q); free(w); return OR_ERR_SHAPE; }
+
+    for (int b = 0; b < B; ++b) {
+        int32_t* ot = out_tokens + (int64_t)b * G1;
+        for (int j = 0; j < G1; ++j) ot[j] = -1;
+        out_accept_len[b] = -1;
+        for (int j = 0; j < gamma; ++j) {
+            if (px) px[(int64_t)b * gamma + j] = NAN;
+            if (qx) qx[(int64_t)b * gamma + j] = NAN;
+            if (margin) margin[(int64_t)b * gamma + j] = NAN;
+        }
+        if (resid_mass) resid_mass[b] = NAN;
+        if (cdf_lo) cdf_lo[b] = NAN;
+        if (cdf_hi) cdf_hi[b] = NAN;
+        if (u_draw) u_draw[b] = NAN;
+        if (events) events[b] = 0;
+        int ev = 0;
+
+        /* validate the request */
+        int st = OR_OK;
+        int ell = verify_len ? verify_len[b] : gamma;
+        const int32_t* x = tokens + (int64_t)b * gamma;
+        const float* u = uniforms ? uniforms + (int64_t)b * G2 : NULL;
+        if (ell < 0 || ell > gamma) st = OR_ERR_VERIFY_LEN;
+        if (st == OR_OK)
+            for (int j = 0; j < ell; ++j)
+                if (x[j] < 0 || x[j] >= V) { st = OR_ERR_TOKEN; break; }
+        if (st == OR_OK && T > 0.0) {
+            for (int j = 0; j < ell; ++j)
+                if (!uniform_ok(u[j])) st = OR_ERR_UNIFORM;
+            if (!uniform_ok(u[gamma]) || !uniform_ok(u[gamma + 1])) st = OR_ERR_UNIFORM;
+        }
+
+        if (st == OR_OK && T == 0.0) {
+            /* Greedy: accept while x_j equals the target argmax of row j. */
+            int32_t am[64];
+            for (int j = 0; j <= ell && st == OR_OK; ++j)
+                st = row_argmax(target, dtype, ((int64_t)b * G1 + j) * V, V, &am[j]);
+            if (st == OR_OK) {
+                int n = 0;
+                while (n < ell && x[n] == am[n]) ++n;
+                for (int j = 0; j < n; ++j) ot[j] = x[j];
+                ot[n] = am[n];
+                out_accept_len[b] = n;
+            }
+        } else if (st == OR_OK) {
+            /* Every needed row must be valid: target 0..ell, draft 0..ell-1. */
+            double pxv[64], qxv[64];
+            for (int j = 0; j <= ell && st == OR_OK; ++j) {
+                st = row_softmax(target, dtype, ((int64_t)b * G1 + j) * V, V, T, p);
+                if (st == OR_OK && j < ell) {
+                    pxv[j] = p[x[j]];
+                    st = row_softmax(draft, dtype, ((int64_t)b * gamma + j) * V, V, T, q);
+                    if (st == OR_OK) qxv[j] = q[x[j]];
+                }
+            }
+            if (st == OR_OK) {
+                for (int j = 0; j < ell; ++j) {
+                    if (px) px[(int64_t)b * gamma + j] = pxv[j];
+                    if (qx) qx[(int64_t)b * gamma + j] = qxv[j];
+                }
+                /* [US] eq. (acceptance): accept x_j with probability
+                 * min(1, p/q); the first rejection ends the prefix. */
+                int n = 0;
+                while (n < ell) {
+                    double uj = (double)u[n];
+                    if (margin) margin[(int64_t)b * gamma + n] = fabs(uj - pxv[n] / qxv[n]);
+                    if (uj * qxv[n] < pxv[n]) ++n;
+                    else break;
+                }
+                for (int j = 0; j < n; ++j) ot[j] = x[j];
+
+                /* The emitted token at position n. */
+                double ud;
+                row_softmax(target, dtype, ((int64_t)b * G1 + n) * V, V, T, p);
+                if (n < ell) {
+                    /* [BL] residual: w = max(p_n - q_n, 0) */
+                    row_softmax(draft, dtype, ((int64_t)b * gamma + n) * V, V, T, q);
+                    double W = 0.0;
+                    for (int v = 0; v < V; ++v) {
+                        double d = p[v] - q[v];
+                        w[v] = d > 0.0 ? d : 0.0;
+                        W += w[v];
+                    }
+                    if (!(W > 0.0)) {
+                        ev |= EV_RESIDUAL_EMPTY;
+                        for (int v = 0; v < V; ++v) w[v] = p[v];
+                    }
+                    ud = (double)u[gamma];
+                } else {
+                    /* bonus token from p of target row ell */
+                    for (int v = 0; v < V; ++v) w[v] = p[v];
+                    ud = (double)u[gamma + 1];
+                }
+                double lo = NAN, hi = NAN, W = 0.0;
+                for (int v = 0; v < V; ++v) W += w[v];
+                int32_t tok = inverse_cdf(w, V, ud, &lo, &hi, &ev);
+                ot[n] = tok;
+                out_accept_len[b] = n;
+                if (resid_mass) resid_mass[b] = W;
+                if (cdf_lo) cdf_lo[b] = lo;
+                if (cdf_hi) cdf_hi[b] = hi;
+                if (u_draw) u_draw[b] = ud;
+            }
+        }
+        if (st != OR_OK) {
+            for (int j = 0; j < G1; ++j) ot[j] = -1;
+            out_accept_len[b] = -1;
+        }
+        if (status) status[b] = st;
+        if (events) events[b] = ev;
+    }
+    free(p);
+    free(q);
+    free(w);
+    return OR_OK;
+}
+
+/* Oracle of the same verification step on probability vectors given directly
+ * (fp64 [B, gamma+1, V] and [B, gamma, V]), used to pin the method on the
+ * pages' worked example without a logit round trip.  Same slots and outputs as
+ * oracle_verify (T > 0 path). */
+int oracle_verify_probs(const double* P, const double* Q, int B, int gamma, int V,
+                        const int32_t* tokens, const double* uniforms, int32_t* out_tokens,
+                        int32_t* out_accept_len, double* resid_mass) {
+    const int G1 = gamma + 1, G2 = gamma + 2;
+    double* w = (double*)malloc(sizeof(double) * (size_t)V);
+    if (!w) return OR_ERR_SHAPE;
+    for (int b = 0; b < B; ++b) {
+        const int32_t* x = tokens + (int64_t)b * gamma;
+        const double* u = uniforms + (int64_t)b * G2;
+        int32_t* ot = out_tokens + (int64_t)b * G1;
+        for (int j = 0; j < G1; ++j) ot[j] = -1;
+        int n = 0;
+        while (n < gamma) {
+            double pj = P[((int64_t)b * G1 + n) * V + x[n]];
+            double qj = Q[((int64_t)b * gamma + n) * V + x[n]];
+            if (u[n] * qj < pj) ++n;
+            else break;
+        }
+        for (int j = 0; j < n; ++j) ot[j] = x[j];
+        const double* pn = P + ((int64_t)b * G1 + n) * V;
+        double ud, W = 0.0;
+        if (n < gamma) {
+            const double* qn = Q + ((int64_t)b * gamma + n) * V;
+            for (int v = 0; v < V; ++v) {
+                double d = pn[v] - qn[v];
+                w[v] = d > 0.0 ? d : 0.0;
+            }
+            ud = u[gamma];
+        } else {
+            for (int v = 0; v < V; ++v) w[v] = pn[v];
+            ud = u[gamma + 1];
+        }
+        for (int v = 0; v < V; ++v) W += w[v];
+        double lo, hi;
+        int ev = 0;
+        ot[n] = inverse_cdf(w, V, ud, &lo, &hi, &ev);
+        out_accept_len[b] = n;
+        if (resid_mass) resid_mass[b] = W;
+    }
+    free(w);
+    return OR_OK;
+}
+
+/* ----------------------------------------------------------------- scheduler */
+
+/* Piecewise-linear round cost C(N): knots (t_i, c_i) with strictly increasing
+ * t, linear between knots, flat beyond both ends.  The evaluation order is
+ * fixed: c_i + ((N - t_i) * (c_{i+1} - c_i)) / (t_{i+1} - t_i). */
+static double cost_at(double N, const double* kt, const double* kc, int nk) {
+    if (N <= kt[0]) return kc[0];
+    if (N >= kt[nk - 1]) return kc[nk - 1];
+    int i = 0;
+    while (!(N < kt[i + 1])) ++i;
+    return kc[i] + ((N - kt[i]) * (kc[i + 1] - kc[i])) / (kt[i + 1] - kt[i]);
+}
+
+int oracle_cost_at(double N, const double* kt, const double* kc, int nk, double* out) {
+    *out = cost_at(N, kt, kc, nk);
+    return OR_OK;
+}
+
+static int check_sched_args(const float* conf, int B, int gamma, const double* kt, const double* kc,
+                            int nk, int min_len) {
+    if (B < 0 || gamma < 0 || min_len < 0 || min_len > gamma) return OR_ERR_SHAPE;
+    if (nk < 1 || nk > 32) return OR_ERR_COST_TABLE;
+    for (int i = 0; i < nk; ++i) {
+        if (!isfinite(kt[i]) || !isfinite(kc[i]) || !(kc[i] > 0.0)) return OR_ERR_COST_TABLE;
+        if (i > 0 && !(kt[i] > kt[i - 1])) return OR_ERR_COST_TABLE;
+    }
+    for (int64_t i = 0; i < (int64_t)B * gamma; ++i)
+        if (!(conf[i] >= 0.0f && conf[i] <= 1.0f)) return OR_ERR_CONFIDENCE;
+    return OR_OK;
+}
+
+/* [AS] eq. (20): s_{b,0} = 1, s_{b,k} = prod_{t<=k} c_{b,t}, products taken
+ * left to right in fp64.  s has gamma + 1 entries per request. */
+static void prefix_survival(const float* conf, int B, int gamma, double* s) {
+    for (int b = 0; b < B; ++b) {
+        double* sb = s + (int64_t)b * (gamma + 1);
+        sb[0] = 1.0;
+        for (int k = 1; k <= gamma; ++k) sb[k] = sb[k - 1] * (double)conf[(int64_t)b * gamma + k - 1];
+    }
+}
+
+/* [AS] eq. (21): estimated progress A_b(n) = sum_{k=0}^{n} s_{b,k}, left to right. */
+static double progress(const double* sb, int n) {
+    double a = 0.0;
+    for (int k = 0; k <= n; ++k) a += sb[k];
+    return a;
+}
+
+typedef struct { double s; int k; int b; } cand_t;
+
+/* Candidate order: survival descending, then shallower position, then lower
+ * request index ([AS] §4.2, top-K with ties broken toward shallower positions). */
+static int cand_cmp(const void* pa, const void* pb) {
+    const cand_t* a = (const cand_t*)pa;
+    const cand_t* c = (const cand_t*)pb;
+    if (a->s > c->s) return -1;
+    if (a->s < c->s) return 1;
+    if (a->k != c->k) return a->k < c->k ? -1 : 1;
+    if (a->b != c->b) return a->b < c->b ? -1 : 1;
+    return 0;
+}
+
+/* Shared set-up of the exact and Algorithm-1 schedulers: survival products,
+ * the base progress at min_len, and the sorted candidate list. */
+static int sched_setup(const float* conf, int B, int gamma, int min_len, double** s_out,
+                       cand_t** c_out, int64_t* nc_out, double* base_out) {
+    double* s = (double*)malloc(sizeof(double) * (size_t)B * (size_t)(gamma + 1) + 8);
+    int64_t nc = (int64_t)B * (gamma - min_len);
+    cand_t* c = (cand_t*)malloc(sizeof(cand_t) * (size_t)(nc > 0 ? nc : 1));
+    if (!s || !c) { free(s); free(c); return OR_ERR_SHAPE; }
+    prefix_survival(conf, B, gamma, s);
+    double base = 0.0;
+    for (int b = 0; b < B; ++b) base += progress(s + (int64_t)b * (gamma + 1), min_len);
+    int64_t i = 0;
+    for (int b = 0; b < B; ++b)
+        for (int k = min_len + 1; k <= gamma; ++k) {
+            c[i].s = s[(int64_t)b * (gamma + 1) + k];
+            c[i].k = k;
+            c[i].b = b;
+            ++i;
+        }
+    qsort(c, (size_t)nc, sizeof(cand_t), cand_cmp);
+    *s_out = s;
+    *c_out = c;
+    *nc_out = nc;
+    *base_out = base;
+    return OR_OK;
+}
+
+/* Exact scan: for every budget N from B(min_len+1) to B(gamma+1), the best
+ * allocation keeps the top-(N - B(min_len+1)) candidates; tau(N) is the
+ * sequential fp64 sum of the base and the sorted survivals, and the selected N
+ * is the first (smallest) strict maximum of tau(N) / C(N)
+ * ([AS] eqs. (21), (23)-(24) with every budget a candidate).
+ * out_gap: relative gap between the best objective and the best one at any
+ * other N (for near-tie flags). */
+int oracle_sched_exact(const float* conf, int B, int gamma, const double* kt, const double* kc,
+                       int nk, int min_len, int32_t* out_len, double* out_obj, double* out_gap) {
+    int st = check_sched_args(conf, B, gamma, kt, kc, nk, min_len);
+    if (st != OR_OK) return st;
+    if (B == 0) return OR_OK;
+    double* s;
+    cand_t* c;
+    int64_t nc;
+    double tau;
+    st = sched_setup(conf, B, gamma, min_len, &s, &c, &nc, &tau);
+    if (st != OR_OK) return st;
+    double N0 = (double)B * (double)(min_len + 1);
+    double best = tau / cost_at(N0, kt, kc, nk);
+    int64_t bestK = 0;
+    double* objs = (double*)malloc(sizeof(double) * (size_t)(nc + 1));
+    objs[0] = best;
+    for (int64_t i = 0; i < nc; ++i) {
+        tau += c[i].s;
+        double obj = tau / cost_at(N0 + (double)(i + 1), kt, kc, nk);
+        objs[i + 1] = obj;
+        if (obj > best) { best = obj; bestK = i + 1; }
+    }
+    double second = -INFINITY;
+    for (int64_t i = 0; i <= nc; ++i)
+        if (i != bestK && objs[i] > second) second = objs[i];
+    for (int b = 0; b < B; ++b) out_len[b] = min_len;
+    for (int64_t i = 0; i < bestK; ++i) out_len[c[i].b] += 1;
+    if (out_obj) *out_obj = best;
+    if (out_gap) *out_gap = nc > 0 ? (best - second) / best : INFINITY;
+    free(objs);
+    free(s);
+    free(c);
+    return OR_OK;
+}
+
+/* [US] §3.5 Algorithm 1 as printed, generalised to a minimum length:
+ * candidates with survival > eps (eps = 0), sorted descending; start with
+ * ell_r = min_len, budget B = R(min_len+1) and tau = sum_r A_r(min_len); take
+ * candidates in order while they extend a contiguous prefix, keeping each one
+ * only while tau / C(budget) strictly improves, and stop at the first one that
+ * does not (reverting it).  j is read as 0-based, so the candidate for depth k
+ * extends ell_r = k - 1 to k. */
+int oracle_sched_alg1(const float* conf, int B, int gamma, const double* kt, const double* kc,
+                      int nk, int min_len, int32_t* out_len) {
+    int st = check_sched_args(conf, B, gamma, kt, kc, nk, min_len);
+    if (st != OR_OK) return st;
+    if (B == 0) return OR_OK;
+    double* s;
+    cand_t* c;
+    int64_t nc;
+    double tau;
+    st = sched_setup(conf, B, gamma, min_len, &s, &c, &nc, &tau);
+    if (st != OR_OK) return st;
+    for (int b = 0; b < B; ++b) out_len[b] = min_len;
+    double budget = (double)B * (double)(min_len + 1);
+    double theta_star = tau / cost_at(budget, kt, kc, nk);
+    const double eps = 0.0;
+    for (int64_t i = 0; i < nc; ++i) {
+        if (!(c[i].s > eps)) continue; /* not a valid candidate */
+        int r = c[i].b;
+        if (out_len[r] != c[i].k - 1) continue; /* non-contiguous prefix: skip */
+        out_len[r] = c[i].k;
+        budget += 1.0;
+        tau += c[i].s;
+        double theta = tau / cost_at(budget, kt, kc, nk);
+        if (theta > theta_star) {
+            theta_star = theta;
+        } else {
+            out_len[r] = c[i].k - 1; /* early stop: throughput saturated */
+            break;
+        }
+    }
+    free(s);
+    free(c);
+    return OR_OK;
+}
+
+/* Brute force over every allocation in [min_len, gamma]^B: tau = sum_b A_b(ell_b),
+ * N = sum_b (ell_b + 1), objective tau / C(N).  Best = largest objective, ties
+ * to the smaller N, then the first in odometer order (request 0 fastest).
+ * out_gap: relative gap to the best objective of any other allocation.
+ * Refuses more than 2^24 allocations. */
+int oracle_sched_brute(const float* conf, int B, int gamma, const double* kt, const double* kc,
+                       int nk, int min_len, int32_t* out_len, double* out_obj, double* out_gap) {
+    int st = check_sched_args(conf, B, gamma, kt, kc, nk, min_len);
+    if (st != OR_OK) return st;
+    if (B == 0) return OR_OK;
+    double count = pow((double)(gamma - min_len + 1), (double)B);
+    if (count > 16777216.0) return OR_ERR_SHAPE;
+    double* s = (double*)malloc(sizeof(double) * (size_t)B * (size_t)(gamma + 1));
+    int32_t* cur = (int32_t*)malloc(sizeof(int32_t) * (size_t)B);
+    prefix_survival(conf, B, gamma, s);
+    for (int b = 0; b < B; ++b) cur[b] = min_len;
+    double best = -INFINITY, second = -INFINITY;
+    int64_t bestN = 0;
+    for (;;) {
+        double tau = 0.0;
+        int64_t N = 0;
+        for (int b = 0; b < B; ++b) {
+            tau += progress(s + (int64_t)b * (gamma + 1), cur[b]);
+            N += cur[b] + 1;
+        }
+        double obj = tau / cost_at((double)N, kt, kc, nk);
+        if (obj > best || (obj == best && N < bestN)) {
+            if (best > second) second = best;
+            best = obj;
+            bestN = N;
+            memcpy(out_len, cur, sizeof(int32_t) * (size_t)B);
+        } else if (obj > second) {
+            second = obj;
+        }
+        int b = 0;
+        while (b < B && cur[b] == gamma) cur[b++] = min_len;
+        if (b == B) break;
+        cur[b] += 1;
+    }
+    if (out_obj) *out_obj = best;
+    if (out_gap) *out_gap = (best - second) / best;
+    free(s);
+    free(cur);
+    return OR_OK;
+}
