@@ -1,0 +1,380 @@
+"""Throughput of batched speculative verification on GB300.
+
+Default workload: block-diffusion verification, B=64 requests per GPU,
+gamma=16 draft tokens, V=131072, bf16 logits, T=1 (synthetic, seeded).  One
+step = one spec_verify call over the whole batch (plan, row statistics,
+accept / first rejection, residual or bonus draw).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun every rank verifies its own
+batch (weak scaling, no collective on the data path); the reported time is
+the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified rows/sec at B=64,γ=16,V=128k bf16; achieved HBM GB/s as % of GB300 peak"
+UNIT = "verified rows/s"
+WORKLOAD = "block_diffusion"
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "row_stats_block_diffusion.md")
+KERNEL_SOURCES = ["speculative_decoding_verification_softmax_gb300/csrc/specv_verify.cu",
+                  "speculative_decoding_verification_softmax_gb300/csrc/specv_common.cuh"]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak_gbs():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the row-statistics kernel from the committed ncu
+    summary, or None if the kernel source changed since the capture."""
+    try:
+        txt = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", txt)
+    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if not m_hash or not m_tr or m_hash.group(1) != kernel_source_hash():
+        return None
+    return float(m_tr.group(1))
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------- distributed
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), \
+        int(os.environ.get("LOCAL_RANK", 0))
+
+
+def reduce_max(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(ms_per_step_max: float, units_per_rank: int, world: int) -> float:
+    """Whole-job throughput: units of all ranks over the slowest rank's time."""
+    return units_per_rank * world / (ms_per_step_max / 1e3)
+
+
+# -------------------------------------------------------------- CPU oracle
+def time_oracle(case, requests: list[int], cores: int) -> float:
+    """Wall time of the oracle over the given requests, split across threads."""
+    from concurrent.futures import ThreadPoolExecutor
+    import oracle
+    chunks = [requests[i::cores] for i in range(cores) if requests[i::cores]]
+
+    def run(rs):
+        for b in rs:
+            oracle.verify(case.target, case.draft, case.dtype, case.draft_tokens, case.verify_len, case.T,
+                          case.uniforms, b0=b, b1=b + 1)
+
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(len(chunks)) as ex:
+        list(ex.map(run, chunks))
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(case, cores: int) -> dict:
+    reqs = list(range(case.B))
+    dt = time_oracle(case, reqs, cores)
+    return {"value": len(reqs) * case.gamma / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"one full batch ({case.B} requests, {case.B * (2 * case.gamma + 1)} logit rows) "
+                      f"of the {WORKLOAD} workload, requests split across {cores} host threads",
+            "seconds": dt}
+
+
+# ------------------------------------------------------------------- main
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import specsynth
+    case = specsynth.make_verify_case(WORKLOAD)
+    cores = os.cpu_count() or 1
+    per_step = min(case.B, cores)
+    W = max(args.warmup, 0)
+    for s in range(W):
+        time_oracle(case, [(s * per_step + i) % case.B for i in range(per_step)], cores)
+    t = 0.0
+    for s in range(args.steps):
+        t += time_oracle(case, [((W + s) * per_step + i) % case.B for i in range(per_step)], cores)
+    ms = t / args.steps * 1e3
+    value = per_step * case.gamma / (ms / 1e3)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": W, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(case),
+            "cpu_baseline": {"kind": "oracle", "cores": cores, "value": value, "unit": UNIT,
+                             "sample": f"{per_step} requests of the {WORKLOAD} batch per step, "
+                                       f"one host thread each"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(case):
+    logit_bytes = case.B * (2 * case.gamma + 1) * case.V * 2
+    return {"workload": f"{WORKLOAD} verify: B={case.B} per GPU, gamma={case.gamma}, V={case.V}, "
+                        f"bf16 logits, T={case.T:g}, verify_len=gamma",
+            "B_per_gpu": case.B, "gamma": case.gamma, "V": case.V, "storage": "bf16",
+            "l2": f"inputs larger than L2 ({logit_bytes / 1e6:.1f} MB of logits read per step)"}
+
+
+def run_ours(args):
+    import torch
+    import specsynth
+    import speculative_decoding_verification_softmax_gb300 as sv
+    from tests import _helpers as H
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    sv.build()
+
+    case = specsynth.make_verify_case(WORKLOAD, seed_logits=300 + 1000 * rank, seed_noise=301 + 1000 * rank,
+                                      seed_tokens=302 + 1000 * rank, seed_uniforms=303 + 1000 * rank)
+    B, gamma, V = case.B, case.gamma, case.V
+    t, d, x, vl, u = H.to_device(case, dev)
+    out_t = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
+    out_n = torch.empty((B,), dtype=torch.int32, device=dev)
+    ws = sv.alloc_verify_workspace(B, gamma, V, sv.BF16, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        sv.verify(t, d, x, vl, case.T, u, out_tokens=out_t, out_accept_len=out_n, workspace=ws)
+
+    W = max(args.warmup, 3)
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize(dev)
+    if sv.read_status(ws) != 0:
+        raise RuntimeError("device status after warm-up")
+
+    # timed region: K steps, events on the launching stream; the row-stats
+    # kernel of each step is bracketed by its own event pair
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(args.steps)]
+    for a, b in pairs:          # create the events before the timed region
+        a.record(stream)
+        b.record(stream)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for a, b in pairs:
+            sv.profile_events(a, b)
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    sv.profile_events(None, None)
+    if world > 1:
+        torch.distributed.barrier()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    ms_max = reduce_max(ms, world, dev)
+    k1_ms = sum(a.elapsed_time(b) for a, b in pairs) / len(pairs)
+    status = sv.read_status(ws)
+    n = out_n.cpu().numpy()
+
+    # end to end through the public API: pinned host inputs -> device -> verify -> host outputs
+    h_t = torch.from_numpy(case.target.view(np.int16)).pin_memory()
+    h_d = torch.from_numpy(case.draft.view(np.int16)).pin_memory()
+    h_x = torch.from_numpy(case.draft_tokens).pin_memory()
+    h_vl = torch.from_numpy(case.verify_len).pin_memory()
+    h_u = torch.from_numpy(case.uniforms).pin_memory()
+    h_ot = torch.empty((B, gamma + 1), dtype=torch.int32).pin_memory()
+    h_on = torch.empty((B,), dtype=torch.int32).pin_memory()
+    tv, dv = t.view(torch.int16), d.view(torch.int16)
+
+    def e2e_step():
+        tv.copy_(h_t, non_blocking=True)
+        dv.copy_(h_d, non_blocking=True)
+        x.copy_(h_x, non_blocking=True)
+        vl.copy_(h_vl, non_blocking=True)
+        u.copy_(h_u, non_blocking=True)
+        step()
+        h_ot.copy_(out_t, non_blocking=True)
+        h_on.copy_(out_n, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, world, dev)
+    h2d = sum(a.numel() * a.element_size() for a in (h_t, h_d, h_x, h_vl, h_u))
+    d2h = h_ot.numel() * 4 + h_on.numel() * 4
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    rows_per_step = B * gamma
+    value = aggregate(ms_max, rows_per_step, world)
+    alg_bytes = B * (2 * gamma + 1) * V * 2                      # row-stats kernel, all rows needed
+    rejected = int((n < gamma).sum())
+    resid_bytes = (2 * rejected + (B - rejected)) * V * 2
+    peak, peak_kind = measured_peak_gbs()
+    achieved = alg_bytes / (k1_ms / 1e3) / 1e9
+    step_gbs = (alg_bytes + resid_bytes) / (ms / 1e3) / 1e9
+    traffic = profiled_traffic()
+    cores = os.cpu_count() or 1
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": W, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": workload_config(case),
+        "hbm": {"gbs_per_gpu": step_gbs, "pct_of_measured_peak": 100.0 * step_gbs / peak,
+                "bytes_per_step": alg_bytes + resid_bytes, "peak_gbs": peak, "peak_kind": peak_kind,
+                "vendor_nominal_gbs": 7900.0},
+        "roofline": {"kernel": "k_row_stats", "bound": "hbm", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": alg_bytes, "avg_launch_ms": k1_ms,
+                     "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})"},
+        "cpu_baseline": cpu_baseline(case, cores),
+        "e2e": {"value": aggregate(e2e_ms, rows_per_step, world), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": sv.kernel_count(B, case.T) * args.steps,
+        "clocks": clk.summary(),
+        "device_status": status,
+        "mean_accept_len": float(n.mean()),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_profile_case(args):
+    """A small case for ncu captures: B requests of the same workload (inputs
+    still larger than L2), a few spec_verify calls, nothing else."""
+    import torch
+    import specsynth
+    import speculative_decoding_verification_softmax_gb300 as sv
+    from tests import _helpers as H
+    sv.build()
+    case = specsynth.make_verify_case(WORKLOAD, B=args.profile_batch)
+    t, d, x, vl, u = H.to_device(case)
+    ws = sv.alloc_verify_workspace(case.B, case.gamma, case.V, sv.BF16)
+    for _ in range(args.warmup + args.steps):
+        sv.verify(t, d, x, vl, case.T, u, workspace=ws)
+    torch.cuda.synchronize()
+    st = sv.read_status(ws)
+    print(json.dumps({"profile_case": WORKLOAD, "B": case.B, "calls": args.warmup + args.steps,
+                      "status": st}))
+    if st != 0:
+        raise SystemExit(1)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--profile-case", action="store_true",
+                    help="run only a small case for ncu (B=--profile-batch)")
+    ap.add_argument("--profile-batch", type=int, default=24)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = ap.parse_args(argv)
+    if args.profile_case:
+        run_profile_case(args)
+    elif args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

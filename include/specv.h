@@ -1,0 +1,197 @@
+/*
+ * specv.h -- C ABI of the GB300 speculative-decoding verification library
+ * (libspecv.so).
+ *
+ * Two operations, both defined on the pages this library restates:
+ *
+ *   spec_verify    batched lossless draft verification.  For each request b
+ *                  and draft position j < ell_b it forms the temperature
+ *                  softmax p of target row j and q of draft row j over the full
+ *                  vocabulary, accepts draft token x_j when u_j * q(x_j) <
+ *                  p(x_j) (i.e. with probability min(1, p/q)), stops at the
+ *                  first rejection n, and emits one more token: a draw from the
+ *                  normalised residual max(p_n - q_n, 0) after a rejection, or a
+ *                  bonus draw from p of target row ell_b when every tested
+ *                  draft was accepted.
+ *                  Sources: "UraionSpec: A Faithful Implementation of
+ *                  Confidence-Scheduled Speculative Decoding" §2.1, eq.
+ *                  (acceptance); "breaking down dspark and its lineage", section
+ *                  "Preserving the target distribution during verification";
+ *                  "AngelSpec" §1 and §4.1 (verified prefix plus one
+ *                  target-generated bonus token).
+ *
+ *   spec_schedule  confidence-scheduled verify lengths.  Prefix survival
+ *                  s_{b,k} = prod_{t<=k} c_{b,t} (s_{b,0} = 1), estimated progress
+ *                  A_b(n) = sum_{k<=n} s_{b,k}, candidates taken in order of
+ *                  survival (ties: shallower position, then lower request), and
+ *                  the budget N = sum_b (ell_b + 1) chosen to maximise
+ *                  tau(N) / C(N) against a piecewise-linear round-cost table.
+ *                  Sources: "AngelSpec" §4.2, eqs. (19)-(24); "UraionSpec" §3.5,
+ *                  Algorithm 1 (hardware-aware prefix scheduler).
+ *
+ * Conventions for every call:
+ *   - All array pointers are DEVICE pointers unless marked host.  The caller
+ *     owns every buffer; the library never allocates or frees device memory.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL
+ *     is the legacy default stream).  No call synchronises the stream except
+ *     spec_read_status.
+ *   - A negative return value is an error detected on the host: nothing was
+ *     launched and no output was written.  Errors found in device data (a bad
+ *     token id, a NaN row, ...) mark the affected request (out_accept_len = -1,
+ *     its tokens -1) and set a sticky status word in the workspace, read with
+ *     spec_read_status.
+ *   - Every device wait in the kernels is bounded; on expiry a kernel records
+ *     SPEC_ERR_TIMEOUT in the status word and returns.
+ */
+#ifndef SPECV_H
+#define SPECV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void* spec_stream_t; /* a cudaStream_t */
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
+
+enum {
+    SPEC_OK = 0,
+    SPEC_ERR_NULL = -1,        /* a required pointer is NULL */
+    SPEC_ERR_SHAPE = -2,       /* B, gamma, V or min_len out of range */
+    SPEC_ERR_ALIGN = -3,       /* a pointer is not aligned to its element size / 16 B */
+    SPEC_ERR_TEMPERATURE = -4, /* temperature not 0 and not in [1e-4, 1e4], or NaN */
+    SPEC_ERR_VERIFY_LEN = -5,  /* device: verify_len[b] outside [0, gamma] */
+    SPEC_ERR_TOKEN = -6,       /* device: draft token outside [0, V) at a tested position */
+    SPEC_ERR_WORKSPACE = -7,   /* workspace smaller than the *_workspace_bytes value */
+    SPEC_ERR_COST_TABLE = -8,  /* cost table: n outside [1, 32], knots not increasing, cost <= 0 */
+    SPEC_ERR_NONFINITE = -9,   /* device: a needed logit row has a NaN, +inf, or no finite value */
+    SPEC_ERR_TIMEOUT = -10,    /* device: a bounded wait expired (results of the call invalid) */
+    SPEC_ERR_CUDA = -11,       /* a CUDA runtime call failed (launch, attribute query) */
+    SPEC_ERR_UNIFORM = -12,    /* device: a used uniform outside [0, 1) */
+    SPEC_ERR_CONFIDENCE = -13  /* device: a confidence outside [0, 1] or NaN */
+};
+
+/* Limits of this build. */
+#define SPEC_MAX_BATCH 4096
+#define SPEC_MAX_GAMMA 32
+#define SPEC_MAX_SCHED_CANDIDATES 16384 /* B * (gamma - min_len) for spec_schedule */
+
+/* ------------------------------------------------------------- verification */
+
+/* Bytes of device workspace spec_verify needs for these sizes (0 if the sizes
+ * are out of range).  Depends only on (B, gamma, V, dt). */
+size_t spec_verify_workspace_bytes(int B, int gamma, int V, spec_dtype dt);
+
+/*
+ * Batched verification of B requests with up to gamma draft tokens each.
+ *
+ *   target_logits  [B, gamma+1, V] row-major, dt; row j of request b holds the
+ *                  target logits for draft position j (row gamma: the position
+ *                  after the last draft).  Aligned to the element size.
+ *   draft_logits   [B, gamma, V] row-major, dt; may be NULL when temperature == 0
+ *                  or gamma == 0 (never read then).
+ *   draft_tokens   [B, gamma] int32; only positions j < ell_b are read.
+ *   verify_len     [B] int32, ell_b in [0, gamma]; NULL means gamma for all.
+ *                  Rows j > ell_b (target) and j >= ell_b (draft) are not read.
+ *   temperature    0 = greedy (accept while x_j == argmax of target row j,
+ *                  lowest index on ties; emit the argmax of row n); otherwise
+ *                  p = softmax(z / T) with T in [1e-4, 1e4].
+ *   uniforms       [B, gamma+2] fp32 in [0,1): slot j < gamma is the accept test
+ *                  of position j, slot gamma the residual draw, slot gamma+1 the
+ *                  bonus draw.  Not read (may be NULL) when temperature == 0.
+ *   out_tokens     [B, gamma+1] int32: x_0..x_{n-1}, then the drawn token at
+ *                  position n, then -1.
+ *   out_accept_len [B] int32: n, the number of accepted drafts (-1 if the
+ *                  request's inputs were invalid).
+ *   workspace      device scratch of at least spec_verify_workspace_bytes(),
+ *                  16-byte aligned; holds the sticky status word.  Its contents
+ *                  need no initialisation.  Two calls sharing one workspace
+ *                  must be ordered on the same stream.
+ * Draws use the inverse CDF: the token is the smallest v whose running sum of
+ * weights exceeds u * (sum of weights).  Returns SPEC_OK or a host-detected
+ * error (nothing launched).  B == 0 returns SPEC_OK without launching.
+ */
+int spec_verify(const void* target_logits, const void* draft_logits, spec_dtype dt, int B,
+                int gamma, int V, const int32_t* draft_tokens, const int32_t* verify_len,
+                float temperature, const float* uniforms, int32_t* out_tokens,
+                int32_t* out_accept_len, void* workspace, size_t workspace_bytes,
+                spec_stream_t stream);
+
+/*
+ * Diagnostics of the last spec_verify that used `workspace` (same B, gamma, V,
+ * dt; stream-ordered after it).  Each output is a device pointer or NULL:
+ *   px, qx      [B, gamma] fp64: p(x_j), q(x_j) for j < ell_b, NaN elsewhere
+ *               (and at temperature 0).
+ *   resid_mass  [B] fp64: the total weight of the final draw, sum_v max(p - q, 0)
+ *               after a rejection, sum_v p_v (= 1 up to rounding) for a bonus
+ *               draw; NaN at temperature 0 or for an invalid request.
+ *   status      [B] int32: per-request status (SPEC_OK or a device error code).
+ */
+int spec_verify_stats(const void* workspace, size_t workspace_bytes, int B, int gamma, int V,
+                      spec_dtype dt, double* px, double* qx, double* resid_mass, int32_t* status,
+                      spec_stream_t stream);
+
+/* --------------------------------------------------------------- scheduling */
+
+/* Piecewise-linear round cost C(N): knots (tokens[i], cost_ms[i]), i < n, with
+ * strictly increasing tokens and positive costs; linear between knots, flat
+ * beyond both ends.  Evaluated in fp64 as
+ *   cost_ms[i] + ((N - tokens[i]) * (cost_ms[i+1] - cost_ms[i])) / (tokens[i+1] - tokens[i])
+ * for tokens[i] <= N < tokens[i+1]. */
+typedef struct {
+    int n;
+    double tokens[32];
+    double cost_ms[32];
+} spec_cost_table;
+
+typedef enum {
+    SPEC_SCHED_EXACT = 0,      /* first budget N that maximises tau(N)/C(N) over every N */
+    SPEC_SCHED_ALGORITHM1 = 1  /* Algorithm 1: add candidates while tau/C strictly improves */
+} spec_sched_mode;
+
+/* Bytes of device workspace spec_schedule needs (its status word). */
+size_t spec_schedule_workspace_bytes(int B, int gamma);
+
+/*
+ * Per-request verify lengths for B requests with gamma draft positions.
+ *   confidence      [B, gamma] fp32 in [0, 1]; confidence[b][k-1] is c_{b,k}.
+ *   cost            HOST pointer, copied by value into the launch.
+ *   min_len         every request keeps at least min_len drafts (0 <= min_len <= gamma).
+ *   out_verify_len  [B] int32 in [min_len, gamma] (all -1 if a confidence is invalid).
+ * Arithmetic is fp64 with a fixed order (left-to-right products and sums, the
+ * budget prefix summed in sorted order), so results are reproducible bit for
+ * bit.  Requires B <= 4096, gamma <= 32, B * (gamma - min_len) <= 16384.
+ */
+int spec_schedule(const float* confidence, int B, int gamma, const spec_cost_table* cost,
+                  int min_len, spec_sched_mode mode, int32_t* out_verify_len, void* workspace,
+                  size_t workspace_bytes, spec_stream_t stream);
+
+/* ------------------------------------------------------------------ status */
+
+/* Synchronises `stream`, reads the sticky device status word of `workspace`
+ * into *status and clears it.  Returns SPEC_OK or SPEC_ERR_CUDA. */
+int spec_read_status(void* workspace, spec_stream_t stream, int* status);
+
+/* A static English description of a status code. */
+const char* spec_status_string(int status);
+
+/* ---------------------------------------------------------------- profiling */
+
+/* Registers two cudaEvent_t handles (as void*) that later spec_verify calls
+ * record on their stream immediately before and after the row-statistics
+ * kernel (the HBM-streaming pass), so a caller can time that kernel alone.
+ * Pass NULL, NULL to stop.  Process-wide setting; not thread-safe. */
+int spec_profile_events(void* before_row_stats, void* after_row_stats);
+
+/* Number of kernels one spec_verify call launches for these arguments
+ * (depends on temperature == 0 and B == 0 only). */
+int spec_verify_kernel_count(int B, float temperature);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECV_H */

@@ -1,0 +1,244 @@
+// Shared device helpers of the verification and scheduling kernels:
+// inline PTX for mbarriers, 1-D bulk copies (cp.async.bulk), NaN-propagating
+// max, the MUFU base-2 exponential, warp reductions, and the workspace layout.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/specv.h"
+
+namespace specv {
+
+// ---------------------------------------------------------------- tunables
+// Bytes of one row chunk: the unit of work of one warp in the streaming pass
+// and of the residual pass.  4 KiB = 2048 bf16 or 1024 fp32 logits.
+constexpr int kChunkBytes = 4096;
+// Row-statistics kernel: warps per CTA and bulk-copy stages per warp.
+constexpr int kStatsWarps = 16;
+constexpr int kStages = 3;
+constexpr int kStatsSmem = kStatsWarps * kStages * kChunkBytes + kStatsWarps * kStages * 8 + 128;
+// Bound on any device wait (nanoseconds of %globaltimer).
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+// ----------------------------------------------------------- workspace
+// Per-request state written by the plan / accept kernels.
+struct ReqState {
+    int ell;     // validated verify length
+    int status;  // SPEC_OK or a device error code
+    int n;       // accepted drafts
+    int mode;    // 0: nothing to draw, 1: residual draw, 2: bonus draw
+    int g_t;     // global row id of the target row of the draw
+    int g_d;     // global row id of the draft row (residual) or -1
+    float u;     // uniform of the draw
+    float M_t;   // integer row scale of the target draw row
+    float M_d;   // integer row scale of the draft draw row
+    float rho_hi, rho_lo;  // S_t / S_d as an unevaluated float pair
+    int pad;
+    double S_t;  // row sum of the target draw row
+};
+
+// Merged statistics of one logit row.
+struct RowStat {
+    float M;   // T > 0: integer-valued scale (max z*c rounded up); T == 0: max logit
+    int arg;   // T == 0: argmax (lowest index); unused for T > 0
+    double S;  // T > 0: sum_v 2^(z_v*c - M); NaN marks an invalid row
+};
+
+struct Layout {
+    int R;        // B * (2*gamma + 1) potential rows
+    int nch;      // chunks per row
+    int CH;       // elements per chunk
+    size_t hdr, row_list, partial, row_stat, req, pq, mass, rchunk, total;
+
+    __host__ __device__ static size_t up(size_t x) { return (x + 255) & ~size_t(255); }
+
+    __host__ __device__ Layout(int B, int gamma, int V, int es) {
+        R = B * (2 * gamma + 1);
+        CH = kChunkBytes / es;
+        nch = (int)(((long long)V + CH - 1) / CH);
+        size_t o = 0;
+        hdr = o;      o = up(o + 256);
+        row_list = o; o = up(o + sizeof(int) * (size_t)R);
+        partial = o;  o = up(o + sizeof(float2) * (size_t)R * (size_t)nch);
+        row_stat = o; o = up(o + sizeof(RowStat) * (size_t)R);
+        req = o;      o = up(o + sizeof(ReqState) * (size_t)B);
+        pq = o;       o = up(o + 2 * sizeof(double) * (size_t)B * (size_t)(gamma > 0 ? gamma : 1));
+        mass = o;     o = up(o + sizeof(double) * (size_t)B);
+        rchunk = o;   o = up(o + sizeof(float) * (size_t)B * (size_t)nch);
+        total = o;
+    }
+};
+
+// Header words (int32) at the start of the workspace.
+constexpr int kHdrStatus = 0;
+constexpr int kHdrRows = 1;
+constexpr int kHdrEvents = 2;
+
+// ------------------------------------------------------------------- PTX
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits for the phase `parity` of `bar`; gives up after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// 1-D bulk copy global -> shared, completion signalled on `bar` (tx bytes).
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Orders this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+    float c;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(c) : "f"(a), "f"(b));
+    return c;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
+    uint32_t c;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(c) : "r"(a), "r"(b));
+    return c;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// ------------------------------------------------------------ reductions
+__device__ __forceinline__ float warp_max_nan(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmax_nan(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ int warp_min_i(int v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Exponent of one logit at scale (c_hi + c_lo) relative to the integer row
+// scale M: t = z*c - M, with the product carried as a float pair.  c_lo > 0
+// keeps t = -inf for z = -inf.
+__device__ __forceinline__ float scaled_exp(float z, float c_hi, float c_lo, float M) {
+    return ex2_approx(fmaf(z, c_lo, fmaf(z, c_hi, -M)));
+}
+
+__device__ __forceinline__ void set_status(int* status_word, int err) {
+    atomicCAS(status_word, 0, err);
+}
+
+// Element range of one chunk of one row, split into an aligned interior that
+// is copied or loaded in 16-byte vectors and scalar head / tail elements.
+struct ChunkSpan {
+    const char* rowp;  // row base
+    int e0, e1;        // chunk element range [e0, e1)
+    int ia, ib;        // aligned interior [ia, ib); ia == ib == e1 if empty
+};
+
+template <int ES>
+__device__ __forceinline__ ChunkSpan chunk_span(const char* rowp, int e0, int e1) {
+    ChunkSpan s;
+    s.rowp = rowp;
+    s.e0 = e0;
+    s.e1 = e1;
+    const uintptr_t p0 = (uintptr_t)(rowp + (size_t)e0 * ES);
+    const uintptr_t p1 = (uintptr_t)(rowp + (size_t)e1 * ES);
+    const uintptr_t A = (p0 + 15) & ~uintptr_t(15);
+    const uintptr_t Z = p1 & ~uintptr_t(15);
+    if (Z > A) {
+        s.ia = e0 + (int)((A - p0) / ES);
+        s.ib = e0 + (int)((Z - p0) / ES);
+    } else {
+        s.ia = s.ib = e1;
+    }
+    return s;
+}
+
+// The single scalar element a lane handles for a span (head: lanes 0-15,
+// tail: lanes 16-31), or -1.  Head <= 15 elements, tail <= 7 (bf16).
+__device__ __forceinline__ int span_scalar_index(const ChunkSpan& s, int lane) {
+    if (lane < 16) {
+        const int i = s.e0 + lane;
+        return i < s.ia ? i : -1;
+    }
+    const int i = s.ib + (lane - 16);
+    return (i < s.e1 && s.ib < s.e1 && s.ia < s.ib) ? i : -1;
+}
+
+template <int ES>
+__device__ __forceinline__ float load_logit(const char* rowp, int i) {
+    if (ES == 2) {
+        const uint32_t h = *(const unsigned short*)(rowp + (size_t)i * 2);
+        return __uint_as_float(h << 16);
+    }
+    return *(const float*)(rowp + (size_t)i * 4);
+}
+
+}  // namespace specv

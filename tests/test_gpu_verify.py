@@ -1,0 +1,190 @@
+"""Parity of the CUDA verification path with the oracle on the GPU.
+
+Every case runs the C ABI through the Python binding on seeded synthetic
+inputs and compares request by request with the fp64 oracle: accept lengths
+and tokens bit-exact except at flagged near-ties, p(x), q(x) and the draw's
+total weight within 1e-5 absolute.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import specsynth
+from tests import _helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import speculative_decoding_verification_softmax_gb300 as sv
+    sv.build()
+
+
+def _run(case, T=None, vl_dev=None, o=None, **kw):
+    T = case.T if T is None else T
+    g = H.gpu_verify(case, T=T, verify_len_dev=vl_dev)
+    if o is None:
+        o = H.oracle_verify(case, T=T)
+    P = H.compare(o, g["tokens"], g["accept_len"], g["px"], g["qx"], g["mass"], g["status"],
+                  greedy=(T == 0), **kw)
+    return g, o, P
+
+
+def _report(name, P):
+    print(f"\n[{name}] requests={P.requests} positions={P.positions} accept_flagged={P.accept_flagged} "
+          f"draw_flagged={P.draw_flagged} max|dp|={P.max_p_err:.2e} max|dmass|={P.max_mass_err:.2e} "
+          f"mismatches={P.mismatches[:5]}")
+
+
+# ------------------------------------------------------------ the workloads
+@pytest.mark.parametrize("name", ["tiny", "mtp_chat", "block_diffusion", "greedy"])
+def test_parity_configs(name):
+    case = specsynth.make_verify_case(name)
+    g, o, P = _run(case)
+    _report(name, P)
+    assert g["device_status"] == 0
+    assert not P.mismatches
+    assert P.max_p_err <= H.PROB_TOL
+    assert P.max_mass_err <= H.PROB_TOL
+    assert P.accept_flagged <= max(0, 1e-4 * P.positions)
+
+
+def test_parity_scheduled_ragged():
+    """Schedule on the GPU (lengths stay on the device), then verify the
+    block-diffusion logits at those ragged lengths."""
+    import torch
+    import speculative_decoding_verification_softmax_gb300 as sv
+    conf = specsynth.make_confidences()
+    cost = specsynth.COST_TABLES["Bprime"]
+    vl_dev, ws = sv.schedule(torch.from_numpy(conf).cuda(), cost, specsynth.SCHED_MIN_LEN)
+    assert sv.read_status(ws) == 0
+    ref = oracle.sched_exact(conf, cost, specsynth.SCHED_MIN_LEN)
+    vl = vl_dev.cpu().numpy()
+    assert (vl == ref["verify_len"]).all()
+    case = specsynth.make_verify_case("block_diffusion")
+    o = H.oracle_verify(case, verify_len=vl)
+    g, o, P = _run(case, vl_dev=vl_dev, o=o)
+    _report("scheduled_ragged", P)
+    assert not P.mismatches
+    assert P.max_p_err <= H.PROB_TOL
+
+
+# -------------------------------------------------------------- edge cases
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("V", [1, 2, 5, 7, 8, 9, 1001, 2047, 2048, 2049, 4097, 65537])
+def test_ragged_vocabularies(dtype, V):
+    case = specsynth.make_verify_case("tiny", B=6, gamma=3, V=V, dtype=dtype, seed_logits=700 + V)
+    g, o, P = _run(case)
+    assert not P.mismatches, P.mismatches[:3]
+    assert P.max_p_err <= H.PROB_TOL
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_unaligned_row_starts(dtype):
+    """Rows whose byte offsets are not 16-byte aligned (V * size % 16 != 0) and a
+    base pointer off a 16-byte boundary exercise the scalar head/tail paths."""
+    import torch
+    import speculative_decoding_verification_softmax_gb300 as sv
+    case = specsynth.make_verify_case("tiny", B=5, gamma=4, V=3001, dtype=dtype)
+    o = H.oracle_verify(case)
+    t, d, x, vl, u = H.to_device(case)
+    tb = torch.empty(t.numel() + 3, dtype=t.dtype, device="cuda")
+    db = torch.empty(d.numel() + 1, dtype=d.dtype, device="cuda")
+    t2 = tb[3:].view(t.shape)
+    d2 = db[1:].view(d.shape)
+    t2.copy_(t)
+    d2.copy_(d)
+    assert t2.data_ptr() % 16 != 0
+    tok, n, ws = sv.verify(t2, d2, x, vl, case.T, u)
+    P = H.compare(o, tok.cpu().numpy(), n.cpu().numpy())
+    assert not P.mismatches
+
+
+@pytest.mark.parametrize("gamma", [0, 1, 32])
+def test_draft_depths(gamma):
+    case = specsynth.make_verify_case("mtp_chat", B=8, gamma=gamma, V=4000)
+    g, o, P = _run(case)
+    assert not P.mismatches
+    if gamma == 0:
+        assert (g["accept_len"] == 0).all()
+
+
+def test_ragged_verify_lengths_including_zero():
+    case = specsynth.make_verify_case("mtp_chat", B=33, gamma=8, V=5000)
+    case.verify_len[:] = np.arange(33) % 9
+    g, o, P = _run(case)
+    assert not P.mismatches
+    assert (g["accept_len"] <= case.verify_len).all()
+
+
+def test_large_batch_small_vocab():
+    case = specsynth.make_verify_case("tiny", B=4096, gamma=4, V=64)
+    g, o, P = _run(case)
+    assert not P.mismatches
+    assert P.accept_flagged <= max(1, 1e-4 * P.positions)
+
+
+def test_equal_rows_accept_everything():
+    case = specsynth.make_verify_case("mtp_chat", B=8, V=3000)
+    case.draft[:] = case.target[:, :-1]
+    case.draft_tokens[:] = specsynth.gumbel_argmax(specsynth.as_f32(case.draft, case.dtype).reshape(-1, case.V),
+                                                   1.0 / case.T, 5).reshape(case.B, case.gamma)
+    g, o, P = _run(case)
+    assert (g["accept_len"] == case.gamma).all()
+    assert not P.mismatches
+
+
+def test_small_temperature_equals_greedy():
+    case = specsynth.make_verify_case("tiny", B=16, V=300, dtype="bf16")
+    tf = specsynth.as_f32(case.target, "bf16")
+    am = tf.argmax(-1)
+    srt = np.sort(tf, -1)
+    ok = (srt[..., -1] - srt[..., -2]) >= 0.1
+    case.draft[:] = case.target[:, :-1]
+    case.draft_tokens[:] = am[:, :-1]
+    case.uniforms[:] = np.minimum(case.uniforms, np.float32(1 - 1e-6))
+    gs = H.gpu_verify(case, T=1e-3)
+    gg = H.gpu_verify(case, T=0.0)
+    keep = ok.all(axis=1)
+    assert keep.sum() >= 4
+    assert (gs["accept_len"][keep] == gg["accept_len"][keep]).all()
+    assert (gs["tokens"][keep] == gg["tokens"][keep]).all()
+
+
+def test_invalid_inputs_marked_per_request():
+    import speculative_decoding_verification_softmax_gb300 as sv
+    case = specsynth.make_verify_case("tiny", B=7)
+    case.verify_len[1] = case.gamma + 1
+    case.draft_tokens[2, 1] = -3
+    case.uniforms[3, case.gamma + 1] = 1.0
+    case.target[4, 2, 17] = np.nan
+    case.draft[5, 0, :] = -np.inf
+    case.target[6, 0, 3] = np.inf
+    g, o, P = _run(case)
+    assert list(g["status"]) == list(o["status"])
+    assert list(o["status"]) == [0, sv.ERR_VERIFY_LEN, sv.ERR_TOKEN, sv.ERR_UNIFORM, sv.ERR_NONFINITE,
+                                 sv.ERR_NONFINITE, sv.ERR_NONFINITE]
+    assert (g["accept_len"][1:] == -1).all() and (g["tokens"][1:] == -1).all()
+    assert g["device_status"] in (sv.ERR_VERIFY_LEN, sv.ERR_TOKEN, sv.ERR_UNIFORM, sv.ERR_NONFINITE)
+
+
+def test_masked_vocabulary_entries():
+    """-inf logits (masked tokens) carry zero probability and are never drawn."""
+    case = specsynth.make_verify_case("mtp_chat", B=8, V=2000)
+    case.target[:, :, 1000:] = specsynth.to_bf16_bits(np.array([-np.inf]))[0]
+    case.draft[:, :, 1500:] = specsynth.to_bf16_bits(np.array([-np.inf]))[0]
+    case.draft_tokens[:] = np.minimum(case.draft_tokens, 1499)
+    g, o, P = _run(case)
+    assert not P.mismatches
+    valid = g["accept_len"] >= 0
+    drawn = g["tokens"][valid, :][np.arange(valid.sum()), g["accept_len"][valid]]
+    assert (drawn < 1000).all()
+
+
+def test_repeated_calls_are_deterministic():
+    case = specsynth.make_verify_case("mtp_chat", B=16, V=32000)
+    a = H.gpu_verify(case)
+    b = H.gpu_verify(case)
+    assert (a["tokens"] == b["tokens"]).all() and (a["accept_len"] == b["accept_len"]).all()
+    assert np.array_equal(a["px"], b["px"], equal_nan=True)
