@@ -17,14 +17,13 @@ constexpr int kChunkBytes = 4096;
 // Row-statistics kernel: warps per CTA and bulk-copy stages per warp.
 constexpr int kStatsWarps = 16;
 constexpr int kStages = 3;
-constexpr int kStatsSmem = kStatsWarps * kStages * kChunkBytes + kStatsWarps * kStages * 8 + 128;
 // Bound on any device wait (nanoseconds of %globaltimer).
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 // ----------------------------------------------------------- workspace
-// Per-request state written by the plan / accept kernels.
+// Per-request state written by the accept kernel, read by the draw kernel.
 struct ReqState {
-    int ell;     // validated verify length
+    int ell;     // verify length (valid only when status == SPEC_OK)
     int status;  // SPEC_OK or a device error code
     int n;       // accepted drafts
     int mode;    // 0: nothing to draw, 1: residual draw, 2: bonus draw
@@ -38,18 +37,44 @@ struct ReqState {
     double S_t;  // row sum of the target draw row
 };
 
-// Merged statistics of one logit row.
-struct RowStat {
-    float M;   // T > 0: integer-valued scale (max z*c rounded up); T == 0: max logit
-    int arg;   // T == 0: argmax (lowest index); unused for T > 0
-    double S;  // T > 0: sum_v 2^(z_v*c - M); NaN marks an invalid row
+// Unevaluated sum hi + lo of two floats (about 48 significant bits).
+struct DF {
+    float hi, lo;
 };
+
+// (a + b) with the rounding error carried (Knuth's TwoSum, then renormalised).
+__device__ __forceinline__ DF df_add(DF a, DF b) {
+    const float s = a.hi + b.hi;
+    const float bb = s - a.hi;
+    const float err = (a.hi - (s - bb)) + (b.hi - bb);
+    const float lo = err + a.lo + b.lo;
+    DF r;
+    r.hi = s + lo;
+    r.lo = lo - (r.hi - s);
+    return r;
+}
+
+__device__ __forceinline__ DF warp_sum_df(DF v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        DF w;
+        w.hi = __shfl_xor_sync(0xffffffffu, v.hi, o);
+        w.lo = __shfl_xor_sync(0xffffffffu, v.lo, o);
+        v = df_add(v, w);
+    }
+    return v;
+}
+
+// 2^e as a float for integer e <= 0 (0 below the normal range).
+__device__ __forceinline__ float pow2_f(int e) {
+    return e < -126 ? 0.0f : __int_as_float((127 + e) << 23);
+}
 
 struct Layout {
     int R;        // B * (2*gamma + 1) potential rows
     int nch;      // chunks per row
     int CH;       // elements per chunk
-    size_t hdr, row_list, partial, row_stat, req, pq, mass, rchunk, total;
+    size_t hdr, partial, req, pq, mass, rchunk, ticket, total;
 
     __host__ __device__ static size_t up(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -59,20 +84,18 @@ struct Layout {
         nch = (int)(((long long)V + CH - 1) / CH);
         size_t o = 0;
         hdr = o;      o = up(o + 256);
-        row_list = o; o = up(o + sizeof(int) * (size_t)R);
         partial = o;  o = up(o + sizeof(float2) * (size_t)R * (size_t)nch);
-        row_stat = o; o = up(o + sizeof(RowStat) * (size_t)R);
         req = o;      o = up(o + sizeof(ReqState) * (size_t)B);
         pq = o;       o = up(o + 2 * sizeof(double) * (size_t)B * (size_t)(gamma > 0 ? gamma : 1));
         mass = o;     o = up(o + sizeof(double) * (size_t)B);
         rchunk = o;   o = up(o + sizeof(float) * (size_t)B * (size_t)nch);
+        ticket = o;   o = up(o + sizeof(int) * (size_t)B);
         total = o;
     }
 };
 
 // Header words (int32) at the start of the workspace.
 constexpr int kHdrStatus = 0;
-constexpr int kHdrRows = 1;
 constexpr int kHdrEvents = 2;
 
 // ------------------------------------------------------------------- PTX
@@ -189,6 +212,11 @@ __device__ __forceinline__ int warp_min_i(int v) {
 __device__ __forceinline__ float scaled_exp(float z, float c_hi, float c_lo, float M) {
     return ex2_approx(fmaf(z, c_lo, fmaf(z, c_hi, -M)));
 }
+
+// Programmatic dependent launch: wait for the preceding kernel's results /
+// allow the next kernel in the stream to be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ void set_status(int* status_word, int err) {
     atomicCAS(status_word, 0, err);

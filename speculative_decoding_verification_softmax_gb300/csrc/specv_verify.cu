@@ -14,19 +14,20 @@
 //   * T == 0 is greedy: accept while x_j is the target argmax.
 //
 // Kernel chain on the caller's stream (no host synchronisation):
-//   k_plan       1 CTA: validates requests, lists the needed logit rows.
-//   k_row_stats  persistent, one CTA per SM: the HBM pass.  Each warp streams
-//                4 KiB row chunks through its own ring of shared-memory stages
-//                filled by 1-D bulk copies (cp.async.bulk + mbarrier) and
-//                writes per-chunk (scale, sum) or (max, argmax) partials.
-//   k_accept     1 CTA per request: merges chunk partials per row (exact
-//                power-of-two rescaling, fp64 sums), computes p(x), q(x), runs
-//                the accept tests with a warp ballot, writes the accepted
-//                prefix and the draw job.
-//   k_resid_sum  one warp per (request, chunk): residual / bonus chunk sums
-//                over the 1-2 draw rows of each request.
-//   k_resid_pick one warp per request: fp64 prefix over chunk sums, then an
-//                in-chunk scan for the inverse-CDF draw.
+//   k_row_stats  persistent, one CTA per SM: the HBM pass.  Each CTA first
+//                derives the needed rows from verify_len (target 0..ell, draft
+//                0..ell-1).  Each warp then streams 4 KiB row chunks through its
+//                own ring of shared-memory stages filled by 1-D bulk copies
+//                (cp.async.bulk + mbarrier) and writes one partial per chunk:
+//                (integer scale, sum of 2^(z*c - scale)) or (max, argmax).
+//   k_accept     one CTA per request: validates the request, merges chunk
+//                partials per row (exact power-of-two rescaling, fp64 sums),
+//                computes p(x), q(x), runs the accept tests with one warp
+//                ballot, writes the accepted prefix and the draw job.
+//   k_draw       one warp per (request, chunk) (T > 0): weights of the 1-2
+//                draw rows summed per chunk; the warp finishing a request's
+//                last chunk takes the fp64 prefix over chunks and scans the
+//                chosen chunk for the inverse-CDF draw.
 #include <math.h>
 
 #include <algorithm>
@@ -36,123 +37,84 @@
 
 namespace specv {
 
-// ===================================================================== plan
-// Per request: validate verify_len, the draft tokens and (T > 0) the used
-// uniforms; count needed rows (target 0..ell, draft 0..ell-1) and list them.
-__global__ void __launch_bounds__(1024) k_plan(const int32_t* __restrict__ verify_len,
-                                               const int32_t* __restrict__ tokens,
-                                               const float* __restrict__ uniforms, int B,
-                                               int gamma, int V, int greedy,
-                                               int32_t* __restrict__ out_tokens,
-                                               int32_t* __restrict__ out_accept_len, char* ws,
-                                               Layout L) {
-    __shared__ int s_warp[32];
+// Descriptor of the chunk that occupies one ring stage.
+struct StageDesc {
+    ChunkSpan sp;
+    int g;  // global row id: target rows [0, B(gamma+1)), then draft rows
+    int c;  // chunk index within the row
+};
+
+constexpr int kStatsThreads = kStatsWarps * 32;
+constexpr size_t kRingBytes = (size_t)kStatsWarps * kStages * kChunkBytes;
+constexpr size_t kBarBytes = (size_t)kStatsWarps * kStages * 8;
+constexpr size_t kDescBytes = (size_t)kStatsWarps * kStages * sizeof(StageDesc);
+constexpr size_t kStatsSmem = kRingBytes + kBarBytes + kDescBytes + (SPEC_MAX_BATCH + 1) * 4 + 128;
+constexpr int kVecPerLane = kChunkBytes / 16 / 32;  // 16-byte vectors per lane in one chunk
+constexpr int kReqThreads = 512;                    // accept / draw kernels
+
+__device__ __forceinline__ bool in01(float u) { return u >= 0.0f && u < 1.0f; }
+
+__device__ __forceinline__ double pow2_d(int e) {
+    return e < -1022 ? 0.0 : __longlong_as_double((long long)(1023 + e) << 52);
+}
+
+// Rows a request needs: target 0..ell and (T > 0) draft 0..ell-1; 0 when
+// verify_len is out of range (the accept kernel marks the request invalid).
+template <bool GREEDY>
+__device__ __forceinline__ int rows_of(const int32_t* verify_len, int b, int gamma) {
+    const int ell = verify_len ? verify_len[b] : gamma;
+    if (ell < 0 || ell > gamma) return 0;
+    return GREEDY ? ell + 1 : 2 * ell + 1;
+}
+
+// prefix[b] = sum of rows of requests < b, prefix[B] = total (whole CTA).
+template <bool GREEDY>
+__device__ void block_row_prefix(const int32_t* verify_len, int B, int gamma, int* prefix) {
+    __shared__ int s_w[32];
     __shared__ int s_total;
-    int* hdr = (int*)(ws + L.hdr);
-    ReqState* req = (ReqState*)(ws + L.req);
-    int* row_list = (int*)(ws + L.row_list);
-    double* pq = (double*)(ws + L.pq);
-    double* mass = (double*)(ws + L.mass);
-
-    const int tid = threadIdx.x;
-    if (tid == 0) {
-        hdr[kHdrStatus] = 0;
-        hdr[kHdrEvents] = 0;
-    }
-    __syncthreads();
-
-    constexpr int PER = 4;  // requests per thread (B <= 4096)
+    constexpr int PER = (SPEC_MAX_BATCH + kStatsThreads - 1) / kStatsThreads;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int cnt[PER];
-    int ells[PER];
     int mine = 0;
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
         const int b = tid * PER + i;
-        cnt[i] = 0;
-        ells[i] = 0;
-        if (b >= B) continue;
-        int st = SPEC_OK;
-        const int ell = verify_len ? verify_len[b] : gamma;
-        if (ell < 0 || ell > gamma) st = SPEC_ERR_VERIFY_LEN;
-        if (st == SPEC_OK)
-            for (int j = 0; j < ell; ++j) {
-                const int x = tokens[(size_t)b * gamma + j];
-                if (x < 0 || x >= V) { st = SPEC_ERR_TOKEN; break; }
-            }
-        if (st == SPEC_OK && !greedy) {
-            const float* u = uniforms + (size_t)b * (gamma + 2);
-            for (int j = 0; j < ell; ++j)
-                if (!(u[j] >= 0.0f && u[j] < 1.0f)) st = SPEC_ERR_UNIFORM;
-            if (!(u[gamma] >= 0.0f && u[gamma] < 1.0f) || !(u[gamma + 1] >= 0.0f && u[gamma + 1] < 1.0f))
-                st = SPEC_ERR_UNIFORM;
-        }
-        ReqState rs;
-        rs.ell = st == SPEC_OK ? ell : 0;
-        rs.status = st;
-        rs.n = -1;
-        rs.mode = 0;
-        rs.g_t = rs.g_d = -1;
-        rs.u = 0.f;
-        rs.M_t = rs.M_d = 0.f;
-        rs.rho_hi = rs.rho_lo = 0.f;
-        rs.pad = 0;
-        rs.S_t = 0.0;
-        req[b] = rs;
-        for (int j = 0; j < gamma; ++j) {
-            pq[2 * ((size_t)b * gamma + j)] = __longlong_as_double(0x7ff8000000000000ll);
-            pq[2 * ((size_t)b * gamma + j) + 1] = __longlong_as_double(0x7ff8000000000000ll);
-        }
-        mass[b] = __longlong_as_double(0x7ff8000000000000ll);
-        if (st != SPEC_OK) {
-            for (int j = 0; j <= gamma; ++j) out_tokens[(size_t)b * (gamma + 1) + j] = -1;
-            out_accept_len[b] = -1;
-            set_status(&hdr[kHdrStatus], st);
-        } else {
-            ells[i] = ell;
-            cnt[i] = greedy ? ell + 1 : 2 * ell + 1;
-        }
+        cnt[i] = b < B ? rows_of<GREEDY>(verify_len, b, gamma) : 0;
         mine += cnt[i];
     }
-
-    // block-wide exclusive scan of `mine`
-    const int lane = tid & 31, warp = tid >> 5;
     int incl = mine;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const int v = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += v;
     }
-    if (lane == 31) s_warp[warp] = incl;
+    if (lane == 31) s_w[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        int w = lane < (int)(blockDim.x >> 5) ? s_warp[lane] : 0;
+        const int w = lane < kStatsWarps ? s_w[lane] : 0;
         int wi = w;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int v = __shfl_up_sync(0xffffffffu, wi, o);
             if (lane >= o) wi += v;
         }
-        s_warp[lane] = wi - w;
+        s_w[lane] = wi - w;
         if (lane == 31) s_total = wi;
     }
     __syncthreads();
-    int off = s_warp[warp] + incl - mine;
-    const int T1 = B * (gamma + 1);
+    int off = s_w[warp] + incl - mine;
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
         const int b = tid * PER + i;
-        if (b >= B || cnt[i] == 0) continue;
-        for (int j = 0; j <= ells[i]; ++j) row_list[off++] = b * (gamma + 1) + j;
-        if (!greedy)
-            for (int j = 0; j < ells[i]; ++j) row_list[off++] = T1 + b * gamma + j;
+        if (b < B) prefix[b] = off;
+        off += cnt[i];
     }
-    if (tid == 0) hdr[kHdrRows] = s_total;
+    if (tid == 0) prefix[B] = s_total;
 }
 
 // ================================================================ row stats
-// One work item = one chunk (kChunkBytes) of one needed row, handled by one
-// warp.  The aligned interior arrives through a bulk copy into the warp's ring
-// stage; up to 15 head and 7 tail elements are loaded directly by lanes.
+// Statistics of one chunk held in a ring stage (aligned interior) plus up to
+// 15 head / 7 tail elements loaded directly by lanes.
 template <int ES, bool GREEDY>
 __device__ __forceinline__ float2 chunk_stats(const char* stage, const ChunkSpan& sp, int lane,
                                               float c_hi, float c_lo) {
@@ -168,20 +130,20 @@ __device__ __forceinline__ float2 chunk_stats(const char* stage, const ChunkSpan
         uint32_t pm = 0xFF80FF80u;  // (-inf, -inf)
         int i = lane;
         for (; i + 32 < nvec; i += 64) {
-            const uint4 a = sm[i], b = sm[i + 32];
-            pm = bf16x2_max_nan(pm, bf16x2_max_nan(bf16x2_max_nan(a.x, a.y), bf16x2_max_nan(a.z, a.w)));
-            pm = bf16x2_max_nan(pm, bf16x2_max_nan(bf16x2_max_nan(b.x, b.y), bf16x2_max_nan(b.z, b.w)));
+            const uint4 x = sm[i], y = sm[i + 32];
+            pm = bf16x2_max_nan(pm, bf16x2_max_nan(bf16x2_max_nan(x.x, x.y), bf16x2_max_nan(x.z, x.w)));
+            pm = bf16x2_max_nan(pm, bf16x2_max_nan(bf16x2_max_nan(y.x, y.y), bf16x2_max_nan(y.z, y.w)));
         }
         if (i < nvec) {
-            const uint4 a = sm[i];
-            pm = bf16x2_max_nan(pm, bf16x2_max_nan(bf16x2_max_nan(a.x, a.y), bf16x2_max_nan(a.z, a.w)));
+            const uint4 x = sm[i];
+            pm = bf16x2_max_nan(pm, bf16x2_max_nan(bf16x2_max_nan(x.x, x.y), bf16x2_max_nan(x.z, x.w)));
         }
         m = fmax_nan(bf16_lo(pm), bf16_hi(pm));
     } else {
         m = -INFINITY;
         for (int i = lane; i < nvec; i += 32) {
-            const float4 a = ((const float4*)stage)[i];
-            m = fmax_nan(m, fmax_nan(fmax_nan(a.x, a.y), fmax_nan(a.z, a.w)));
+            const float4 x = ((const float4*)stage)[i];
+            m = fmax_nan(m, fmax_nan(fmax_nan(x.x, x.y), fmax_nan(x.z, x.w)));
         }
     }
     m = fmax_nan(m, sv);
@@ -194,16 +156,16 @@ __device__ __forceinline__ float2 chunk_stats(const char* stage, const ChunkSpan
             for (int i = lane; i < nvec && best == 0x7fffffff; i += 32) {
                 const int base = sp.ia + i * EPV;
                 if (ES == 2) {
-                    const uint4 a = sm[i];
-                    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+                    const uint4 x = sm[i];
+                    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         if (best == 0x7fffffff && bf16_lo(w[k]) == m) best = base + 2 * k;
                         if (best == 0x7fffffff && bf16_hi(w[k]) == m) best = base + 2 * k + 1;
                     }
                 } else {
-                    const float4 a = ((const float4*)stage)[i];
-                    const float w[4] = {a.x, a.y, a.z, a.w};
+                    const float4 x = ((const float4*)stage)[i];
+                    const float w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
                         if (best == 0x7fffffff && w[k] == m) best = base + k;
@@ -215,133 +177,151 @@ __device__ __forceinline__ float2 chunk_stats(const char* stage, const ChunkSpan
         return make_float2(m, __int_as_float(best));
     }
 
-    // T > 0
+    // T > 0: sum of 2^(z*c - Mc) with the integer scale Mc = ceil(max * c)
     if (m != m || m == INFINITY) return make_float2(__int_as_float(0x7fc00000), 0.f);
     if (m == -INFINITY) return make_float2(-INFINITY, 0.f);
     const float Mc = ceilf(fmaf(m, c_hi, m * c_lo));
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    const float2 ch2 = make_float2(c_hi, c_hi), cl2 = make_float2(c_lo, c_lo), nm2 = make_float2(-Mc, -Mc);
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+    auto pair = [&](float z0, float z1) -> float2 {
+        const float2 z = make_float2(z0, z1);
+        const float2 t = __ffma2_rn(z, cl2, __ffma2_rn(z, ch2, nm2));
+        return make_float2(ex2_approx(t.x), ex2_approx(t.y));
+    };
     if (ES == 2) {
+#pragma unroll 2
         for (int i = lane; i < nvec; i += 32) {
-            const uint4 a = sm[i];
-            a0 += scaled_exp(bf16_lo(a.x), c_hi, c_lo, Mc);
-            a1 += scaled_exp(bf16_hi(a.x), c_hi, c_lo, Mc);
-            a2 += scaled_exp(bf16_lo(a.y), c_hi, c_lo, Mc);
-            a3 += scaled_exp(bf16_hi(a.y), c_hi, c_lo, Mc);
-            a0 += scaled_exp(bf16_lo(a.z), c_hi, c_lo, Mc);
-            a1 += scaled_exp(bf16_hi(a.z), c_hi, c_lo, Mc);
-            a2 += scaled_exp(bf16_lo(a.w), c_hi, c_lo, Mc);
-            a3 += scaled_exp(bf16_hi(a.w), c_hi, c_lo, Mc);
+            const uint4 x = sm[i];
+            acc0 = __fadd2_rn(acc0, pair(bf16_lo(x.x), bf16_hi(x.x)));
+            acc1 = __fadd2_rn(acc1, pair(bf16_lo(x.y), bf16_hi(x.y)));
+            acc0 = __fadd2_rn(acc0, pair(bf16_lo(x.z), bf16_hi(x.z)));
+            acc1 = __fadd2_rn(acc1, pair(bf16_lo(x.w), bf16_hi(x.w)));
         }
     } else {
+#pragma unroll 2
         for (int i = lane; i < nvec; i += 32) {
-            const float4 a = ((const float4*)stage)[i];
-            a0 += scaled_exp(a.x, c_hi, c_lo, Mc);
-            a1 += scaled_exp(a.y, c_hi, c_lo, Mc);
-            a2 += scaled_exp(a.z, c_hi, c_lo, Mc);
-            a3 += scaled_exp(a.w, c_hi, c_lo, Mc);
+            const float4 x = ((const float4*)stage)[i];
+            acc0 = __fadd2_rn(acc0, pair(x.x, x.y));
+            acc1 = __fadd2_rn(acc1, pair(x.z, x.w));
         }
     }
-    if (si >= 0) a0 += scaled_exp(sv, c_hi, c_lo, Mc);
-    const float S = warp_sum((a0 + a1) + (a2 + a3));
+    float S = (acc0.x + acc0.y) + (acc1.x + acc1.y);
+    if (si >= 0) S += scaled_exp(sv, c_hi, c_lo, Mc);
+    S = warp_sum(S);
     return make_float2(Mc, S);
 }
 
 struct StatsArgs {
     const char* target;
     const char* draft;
+    const int32_t* verify_len;
     int B, gamma, V;
     float c_hi, c_lo;
     char* ws;
 };
 
 template <int ES, bool GREEDY>
-__global__ void __launch_bounds__(kStatsWarps * 32, 1) k_row_stats(StatsArgs a, Layout L) {
+__global__ void __launch_bounds__(kStatsThreads, 1) k_row_stats(StatsArgs a, Layout L) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 127) & ~uintptr_t(127));
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     unsigned char* ring = smem + (size_t)warp * kStages * kChunkBytes;
-    uint64_t* bars = (uint64_t*)(smem + (size_t)kStatsWarps * kStages * kChunkBytes) + warp * kStages;
-
+    uint64_t* bars = (uint64_t*)(smem + kRingBytes) + warp * kStages;
+    StageDesc* desc = (StageDesc*)(smem + kRingBytes + kBarBytes) + warp * kStages;
+    int* prefix = (int*)(smem + kRingBytes + kBarBytes + kDescBytes);
     int* hdr = (int*)(a.ws + L.hdr);
-    const int* row_list = (const int*)(a.ws + L.row_list);
     float2* partial = (float2*)(a.ws + L.partial);
 
+    if (blockIdx.x == 0 && tid == 0) {  // per-call reset of the status words
+        hdr[kHdrStatus] = 0;
+        hdr[kHdrEvents] = 0;
+    }
     if (lane == 0) {
         for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
         fence_mbar_init();
     }
-    __syncwarp();
+    block_row_prefix<GREEDY>(a.verify_len, a.B, a.gamma, prefix);
+    __syncthreads();
+    pdl_trigger();
 
-    const long long total = (long long)hdr[kHdrRows] * L.nch;
-    const long long W = (long long)gridDim.x * kStatsWarps;
-    const long long first = (long long)blockIdx.x * kStatsWarps + warp;
+    const int nch = L.nch;
+    const long long total = (long long)prefix[a.B] * nch;
+    const int W = gridDim.x * kStatsWarps;
+    const int gw = blockIdx.x * kStatsWarps + warp;
+    if (gw >= total) return;
+    const long long count = (total - gw + W - 1) / W;  // items of this warp
+    const int Wq = W / nch, Wr = W - Wq * nch;
     const int T1 = a.B * (a.gamma + 1);
 
-    auto span_of = [&](long long item, int& g, int& c) -> ChunkSpan {
-        const int r = (int)(item / L.nch);
-        c = (int)(item - (long long)r * L.nch);
-        g = row_list[r];
+    // issue cursor (lane 0): compact row index, chunk, request of the row
+    int ir = gw / nch, ic = gw - (gw / nch) * nch, rb = 0;
+    auto issue = [&](int s) -> bool {
+        while (prefix[rb + 1] <= ir) ++rb;
+        const int k = ir - prefix[rb], cnt = prefix[rb + 1] - prefix[rb];
+        const int ell = GREEDY ? cnt - 1 : (cnt - 1) >> 1;
+        const int g = k <= ell ? rb * (a.gamma + 1) + k : T1 + rb * a.gamma + (k - ell - 1);
         const char* rowp = g < T1 ? a.target + (size_t)g * a.V * ES
                                   : a.draft + (size_t)(g - T1) * a.V * ES;
-        const int e0 = c * L.CH;
-        const int e1 = min(a.V, e0 + L.CH);
-        return chunk_span<ES>(rowp, e0, e1);
-    };
-    auto issue = [&](int s, long long item) {
-        int g, c;
-        const ChunkSpan sp = span_of(item, g, c);
-        if (sp.ia < sp.ib && lane == 0) {
-            const uint32_t bytes = (uint32_t)((sp.ib - sp.ia) * ES);
+        const int e0 = ic * L.CH;
+        StageDesc d;
+        d.sp = chunk_span<ES>(rowp, e0, min(a.V, e0 + L.CH));
+        d.g = g;
+        d.c = ic;
+        desc[s] = d;
+        const bool copy = d.sp.ia < d.sp.ib;
+        if (copy) {
+            const uint32_t bytes = (uint32_t)((d.sp.ib - d.sp.ia) * ES);
             fence_proxy_async_smem();
             mbar_arrive_expect_tx(&bars[s], bytes);
-            bulk_g2s(ring + (size_t)s * kChunkBytes, sp.rowp + (size_t)sp.ia * ES, bytes, &bars[s]);
+            bulk_g2s(ring + (size_t)s * kChunkBytes, rowp + (size_t)d.sp.ia * ES, bytes, &bars[s]);
         }
-        return sp.ia < sp.ib;
+        ic += Wr;
+        ir += Wq;
+        if (ic >= nch) {
+            ic -= nch;
+            ++ir;
+        }
+        return copy;
     };
 
-    uint32_t phase = 0;     // bit s: parity of the next wait on stage s
-    uint32_t pending = 0;   // bit s: a copy is in flight on stage s
+    uint32_t pending = 0;  // bit s: a copy is in flight on stage s
+    uint32_t phase = 0;    // bit s: parity of the next wait on stage s
+    long long issued = 0;
 #pragma unroll 1
-    for (int s = 0; s < kStages; ++s) {
-        const long long item = first + (long long)s * W;
-        if (item < total && issue(s, item)) pending |= 1u << s;
+    for (int s = 0; s < kStages && issued < count; ++s, ++issued) {
+        bool c = false;
+        if (lane == 0) c = issue(s);
+        if (__shfl_sync(0xffffffffu, c, 0)) pending |= 1u << s;
     }
+    __syncwarp();
 
     int s = 0;
-    bool timed_out = false;
 #pragma unroll 1
-    for (long long item = first; item < total; item += W) {
-        int g, c;
-        const ChunkSpan sp = span_of(item, g, c);
-        const unsigned char* stage = ring + (size_t)s * kChunkBytes;
+    for (long long done = 0; done < count; ++done) {
+        const StageDesc d = desc[s];
         if (pending & (1u << s)) {
             if (!mbar_wait_bounded(&bars[s], (phase >> s) & 1u)) {
-                timed_out = true;
-                break;
+                // record the failure and let this warp's copies in flight land
+                if (lane == 0) set_status(&hdr[kHdrStatus], SPEC_ERR_TIMEOUT);
+                for (int k = 0; k < kStages; ++k)
+                    if (k != s && (pending & (1u << k))) mbar_wait_bounded(&bars[k], (phase >> k) & 1u);
+                return;
             }
             phase ^= 1u << s;
             pending &= ~(1u << s);
         }
-        const float2 r = chunk_stats<ES, GREEDY>((const char*)stage, sp, lane, a.c_hi, a.c_lo);
-        if (lane == 0) partial[(size_t)g * L.nch + c] = r;
+        const float2 r = chunk_stats<ES, GREEDY>((const char*)(ring + (size_t)s * kChunkBytes), d.sp, lane,
+                                                 a.c_hi, a.c_lo);
+        if (lane == 0) partial[(size_t)d.g * nch + d.c] = r;
         __syncwarp();
-        const long long next = item + (long long)kStages * W;
-        if (next < total && issue(s, next)) pending |= 1u << s;
-        s = (s + 1 == kStages) ? 0 : s + 1;
-    }
-
-    if (timed_out) {
-        // Record the failure, let copies in flight land (bounded), and mark
-        // every item this warp did not finish as invalid.
-        if (lane == 0) set_status(&hdr[kHdrStatus], SPEC_ERR_TIMEOUT);
-        for (int k = 0; k < kStages; ++k)
-            if (pending & (1u << k)) mbar_wait_bounded(&bars[k], (phase >> k) & 1u);
-        for (long long item = first; item < total; item += W) {
-            const int r = (int)(item / L.nch);
-            const int c = (int)(item - (long long)r * L.nch);
-            if (lane == 0)
-                partial[(size_t)row_list[r] * L.nch + c] = make_float2(__int_as_float(0x7fc00000), 0.f);
+        if (issued < count) {
+            bool c = false;
+            if (lane == 0) c = issue(s);
+            if (__shfl_sync(0xffffffffu, c, 0)) pending |= 1u << s;
+            ++issued;
         }
+        __syncwarp();
+        s = (s + 1 == kStages) ? 0 : s + 1;
     }
 }
 
@@ -350,6 +330,7 @@ struct AcceptArgs {
     const char* target;
     const char* draft;
     const int32_t* tokens;
+    const int32_t* verify_len;
     const float* uniforms;
     int32_t* out_tokens;
     int32_t* out_accept_len;
@@ -358,116 +339,190 @@ struct AcceptArgs {
     char* ws;
 };
 
-// Merge the chunk partials of row g into a RowStat.
+// Merge the chunk partials of one row.  T > 0: M = max of the chunks'
+// integer scales, S = sum_c S_c * 2^(M_c - M) with exact power-of-two rescaling
+// and a two-float accumulator.  T == 0: (max, lowest argmax).  Returns false
+// for an invalid row.
 template <bool GREEDY>
-__device__ __forceinline__ RowStat merge_row(const float2* part, int nch, int lane) {
-    RowStat rs;
-    rs.arg = 0;
+__device__ __forceinline__ bool merge_row(const float2* part, int nch, int lane, float& M, DF& S, int& arg) {
     if (GREEDY) {
         float best = -INFINITY;
-        int arg = 0x7fffffff;
+        int ix = 0x7fffffff;
         bool bad = false;
         for (int c = lane; c < nch; c += 32) {
             const float2 p = part[c];
-            const int ix = __float_as_int(p.y);
+            const int i = __float_as_int(p.y);
             if (p.x != p.x) bad = true;
-            else if (p.x > best || (p.x == best && ix < arg)) { best = p.x; arg = ix; }
+            else if (p.x > best || (p.x == best && i < ix)) { best = p.x; ix = i; }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-            const int oa = __shfl_xor_sync(0xffffffffu, arg, o);
-            if (ob > best || (ob == best && oa < arg)) { best = ob; arg = oa; }
+            const int oi = __shfl_xor_sync(0xffffffffu, ix, o);
+            if (ob > best || (ob == best && oi < ix)) { best = ob; ix = oi; }
         }
         bad = __any_sync(0xffffffffu, bad);
-        rs.M = best;
-        rs.arg = arg;
-        rs.S = (bad || !(fabsf(best) <= 3.402823466e38f)) ? __longlong_as_double(0x7ff8000000000000ll) : 1.0;
-        return rs;
+        M = best;
+        arg = ix;
+        S.hi = 1.f;
+        S.lo = 0.f;
+        return !bad && fabsf(best) <= 3.402823466e38f;
     }
-    float M = -INFINITY;
-    for (int c = lane; c < nch; c += 32) M = fmax_nan(M, part[c].x);
-    M = warp_max_nan(M);
-    rs.M = M;
-    if (M != M || M == -INFINITY) {
-        rs.S = __longlong_as_double(0x7ff8000000000000ll);
-        return rs;
-    }
-    double S = 0.0;
+    float m = -INFINITY;
+    float2 keep[4];
+    int nk = 0;
     for (int c = lane; c < nch; c += 32) {
         const float2 p = part[c];
+        if (nk < 4) keep[nk++] = p;
+        m = fmax_nan(m, p.x);
+    }
+    m = warp_max_nan(m);
+    M = m;
+    arg = 0;
+    if (m != m || m == -INFINITY) return false;
+    DF acc = {0.f, 0.f};
+    int k = 0;
+    for (int c = lane; c < nch; c += 32, ++k) {
+        const float2 p = k < 4 ? keep[k] : part[c];
         if (p.x != -INFINITY) {
-            // M and p.x are integer-valued floats: the rescale is an exact power of two
-            const float d = p.x - M;
-            const int e = d < -1000.f ? -1000 : (int)d;
-            S += ldexp((double)p.y, e);
+            // both scales are integer-valued: the rescale is an exact power of two
+            const float d = p.x - m;
+            const float v = p.y * pow2_f(d < -1000.f ? -1000 : (int)d);
+            acc = df_add(acc, DF{v, 0.f});
         }
     }
-    rs.S = warp_sum_d(S);
-    return rs;
+    S = warp_sum_df(acc);
+    return S.hi > 0.f && S.hi <= 3.0e38f;
+}
+
+// p = e / (S.hi + S.lo) in fp32
+__device__ __forceinline__ float div_df(float e, DF S) {
+    const float q = e / S.hi;
+    return fmaf(-q, S.lo / S.hi, q);
 }
 
 template <int ES, bool GREEDY>
-__global__ void __launch_bounds__(128) k_accept(AcceptArgs a, Layout L) {
-    const int b = blockIdx.x;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+__global__ void __launch_bounds__(kReqThreads) k_accept(AcceptArgs a, Layout L) {
+    constexpr int NW = kReqThreads / 32;
+    const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    __shared__ float s_M[2 * SPEC_MAX_GAMMA + 1];
+    __shared__ DF s_S[2 * SPEC_MAX_GAMMA + 1];
+    __shared__ int s_arg[2 * SPEC_MAX_GAMMA + 1];
+    __shared__ float s_zt[SPEC_MAX_GAMMA], s_zd[SPEC_MAX_GAMMA];
+    __shared__ int s_status;
     int* hdr = (int*)(a.ws + L.hdr);
     ReqState* req = (ReqState*)(a.ws + L.req);
     const float2* partial = (const float2*)(a.ws + L.partial);
-    RowStat* rstat = (RowStat*)(a.ws + L.row_stat);
     double* pq = (double*)(a.ws + L.pq);
-    __shared__ int s_bad;
+    const int G1 = a.gamma + 1, T1 = a.B * G1;
+    const int ell = a.verify_len ? a.verify_len[b] : a.gamma;
+    const bool ell_ok = ell >= 0 && ell <= a.gamma;
 
-    ReqState rs = req[b];
-    if (rs.status != SPEC_OK) return;
-    const int ell = rs.ell, G1 = a.gamma + 1, T1 = a.B * G1;
-    if (threadIdx.x == 0) s_bad = 0;
-    __syncthreads();
-
-    const int nrows = GREEDY ? ell + 1 : 2 * ell + 1;
-    for (int r = warp; r < nrows; r += 4) {
-        const int g = r <= ell ? b * G1 + r : T1 + b * a.gamma + (r - ell - 1);
-        const RowStat st = merge_row<GREEDY>(partial + (size_t)g * L.nch, L.nch, lane);
+    int st = SPEC_OK;
+    if (warp == 0) {
+        // caller inputs only (ready before the streaming kernel started):
+        // validation and the gathers of z at the (clamped) draft tokens
+        if (!ell_ok) st = SPEC_ERR_VERIFY_LEN;
+        const int j = lane;
+        int x = 0;
+        float uj = 0.f, ug = 0.f, ub = 0.f;
+        if (ell_ok && j < ell) x = a.tokens[(size_t)b * a.gamma + j];
+        if (!GREEDY && ell_ok) {
+            const float* u = a.uniforms + (size_t)b * (a.gamma + 2);
+            if (j < ell) uj = u[j];
+            if (j == 0) {
+                ug = u[a.gamma];
+                ub = u[a.gamma + 1];
+            }
+        }
+        const bool xok = x >= 0 && x < a.V;
+        if (!GREEDY && ell_ok && j < ell) {
+            const int xc = xok ? x : 0;
+            s_zt[j] = load_logit<ES>(a.target + (size_t)(b * G1 + j) * a.V * ES, xc);
+            s_zd[j] = load_logit<ES>(a.draft + (size_t)(b * a.gamma + j) * a.V * ES, xc);
+        }
+        if (st == SPEC_OK && !__all_sync(0xffffffffu, xok)) st = SPEC_ERR_TOKEN;
+        if (st == SPEC_OK && !GREEDY) {
+            bool uok = in01(uj);
+            if (j == 0) uok = uok && in01(ug) && in01(ub);
+            if (!__all_sync(0xffffffffu, uok)) st = SPEC_ERR_UNIFORM;
+        }
+    }
+    pdl_wait();  // the streaming kernel's partials and status word
+    pdl_trigger();
+    if (warp == 0) {
+        if (hdr[kHdrStatus] == SPEC_ERR_TIMEOUT) st = SPEC_ERR_TIMEOUT;
         if (lane == 0) {
-            rstat[g] = st;
-            if (st.S != st.S) s_bad = 1;
+            s_status = st;
+            ((int*)(a.ws + L.ticket))[b] = 0;  // completion ticket of the draw kernel
+        }
+    } else if (ell_ok) {
+        // row merges: target rows 0..ell, then draft rows 0..ell-1
+        const int nrows = GREEDY ? ell + 1 : 2 * ell + 1;
+        for (int r = warp - 1; r < nrows; r += NW - 1) {
+            const int g = r <= ell ? b * G1 + r : T1 + b * a.gamma + (r - ell - 1);
+            float M;
+            DF S;
+            int arg;
+            const bool ok = merge_row<GREEDY>(partial + (size_t)g * L.nch, L.nch, lane, M, S, arg);
+            if (lane == 0) {
+                s_M[r] = M;
+                s_S[r] = ok ? S : DF{__int_as_float(0x7fc00000), 0.f};  // NaN marks an invalid row
+                s_arg[r] = arg;
+            }
         }
     }
     __syncthreads();
     if (warp != 0) return;
 
-    const int32_t* x = a.tokens + (size_t)b * a.gamma;
+    st = s_status;
+    if (st == SPEC_OK) {
+        const int nrows = GREEDY ? ell + 1 : 2 * ell + 1;
+        bool bad = false;
+        for (int r = lane; r < nrows; r += 32) bad |= s_S[r].hi != s_S[r].hi;
+        if (__any_sync(0xffffffffu, bad)) st = SPEC_ERR_NONFINITE;
+    }
     int32_t* ot = a.out_tokens + (size_t)b * G1;
-    if (s_bad) {
-        for (int j = lane; j <= a.gamma; j += 32) ot[j] = -1;
+    const int j = lane;
+    if (st != SPEC_OK) {
+        for (int k = lane; k <= a.gamma; k += 32) ot[k] = -1;
+        for (int k = lane; k < a.gamma; k += 32) {
+            pq[2 * ((size_t)b * a.gamma + k)] = __longlong_as_double(0x7ff8000000000000ll);
+            pq[2 * ((size_t)b * a.gamma + k) + 1] = __longlong_as_double(0x7ff8000000000000ll);
+        }
         if (lane == 0) {
             a.out_accept_len[b] = -1;
-            req[b].status = SPEC_ERR_NONFINITE;
-            set_status(&hdr[kHdrStatus], SPEC_ERR_NONFINITE);
+            ReqState o;
+            o.ell = 0;
+            o.status = st;
+            o.n = -1;
+            o.mode = 0;
+            req[b] = o;
+            ((double*)(a.ws + L.mass))[b] = __longlong_as_double(0x7ff8000000000000ll);
+            set_status(&hdr[kHdrStatus], st);
         }
         return;
     }
 
-    // accept tests, one lane per position (gamma <= 32)
+    // accept tests, one lane per position (gamma <= 32): u * q(x) < p(x)
+    const int32_t* x = a.tokens + (size_t)b * a.gamma;
     bool acc = true;
-    const int j = lane;
+    double pxd = __longlong_as_double(0x7ff8000000000000ll), qxd = pxd;
     if (j < ell) {
-        const int xj = x[j];
-        const int gt = b * G1 + j;
         if (GREEDY) {
-            acc = xj == rstat[gt].arg;
+            acc = x[j] == s_arg[j];
         } else {
-            const int gd = T1 + b * a.gamma + j;
-            const RowStat st = rstat[gt], sd = rstat[gd];
-            const float zt = load_logit<ES>(a.target + (size_t)gt * a.V * ES, xj);
-            const float zd = load_logit<ES>(a.draft + (size_t)(gd - T1) * a.V * ES, xj);
-            const double px = (double)scaled_exp(zt, a.c_hi, a.c_lo, st.M) / st.S;
-            const double qx = (double)scaled_exp(zd, a.c_hi, a.c_lo, sd.M) / sd.S;
-            pq[2 * ((size_t)b * a.gamma + j)] = px;
-            pq[2 * ((size_t)b * a.gamma + j) + 1] = qx;
-            const double u = (double)a.uniforms[(size_t)b * (a.gamma + 2) + j];
-            acc = u * qx < px;
+            const float px = div_df(scaled_exp(s_zt[j], a.c_hi, a.c_lo, s_M[j]), s_S[j]);
+            const float qx = div_df(scaled_exp(s_zd[j], a.c_hi, a.c_lo, s_M[ell + 1 + j]), s_S[ell + 1 + j]);
+            const float u = a.uniforms[(size_t)b * (a.gamma + 2) + j];
+            acc = __fmul_rn(u, qx) < px;
+            pxd = px;
+            qxd = qx;
         }
+    }
+    if (j < a.gamma) {
+        pq[2 * ((size_t)b * a.gamma + j)] = pxd;
+        pq[2 * ((size_t)b * a.gamma + j) + 1] = qxd;
     }
     const unsigned rej = __ballot_sync(0xffffffffu, !acc);
     const int n = rej ? min(__ffs(rej) - 1, ell) : ell;
@@ -477,39 +532,40 @@ __global__ void __launch_bounds__(128) k_accept(AcceptArgs a, Layout L) {
     }
     if (lane == 0) {
         a.out_accept_len[b] = n;
-        req[b].n = n;
+        ((double*)(a.ws + L.mass))[b] = __longlong_as_double(0x7ff8000000000000ll);
+        ReqState o;
+        o.ell = ell;
+        o.status = SPEC_OK;
+        o.n = n;
+        o.mode = 0;
+        o.g_t = b * G1 + n;
+        o.g_d = -1;
+        o.u = 0.f;
+        o.M_t = s_M[n];
+        o.M_d = 0.f;
+        o.rho_hi = o.rho_lo = 0.f;
+        o.pad = 0;
+        o.S_t = (double)s_S[n].hi + (double)s_S[n].lo;
         if (GREEDY) {
-            ot[n] = rstat[b * G1 + n].arg;
+            ot[n] = s_arg[n];
+        } else if (n < ell) {
+            o.mode = 1;
+            o.g_d = T1 + b * a.gamma + n;
+            o.M_d = s_M[ell + 1 + n];
+            const double rho = o.S_t / ((double)s_S[ell + 1 + n].hi + (double)s_S[ell + 1 + n].lo);
+            o.rho_hi = (float)rho;
+            o.rho_lo = (float)(rho - (double)o.rho_hi);
+            o.u = a.uniforms[(size_t)b * (a.gamma + 2) + a.gamma];
         } else {
-            const int gt = b * G1 + n;
-            const RowStat st = rstat[gt];
-            ReqState o = rs;
-            o.n = n;
-            o.g_t = gt;
-            o.M_t = st.M;
-            o.S_t = st.S;
-            if (n < ell) {
-                const int gd = T1 + b * a.gamma + n;
-                const RowStat sd = rstat[gd];
-                o.mode = 1;
-                o.g_d = gd;
-                o.M_d = sd.M;
-                const double rho = st.S / sd.S;
-                o.rho_hi = (float)rho;
-                o.rho_lo = (float)(rho - (double)o.rho_hi);
-                o.u = a.uniforms[(size_t)b * (a.gamma + 2) + a.gamma];
-            } else {
-                o.mode = 2;
-                o.g_d = -1;
-                o.u = a.uniforms[(size_t)b * (a.gamma + 2) + a.gamma + 1];
-            }
-            req[b] = o;
+            o.mode = 2;
+            o.u = a.uniforms[(size_t)b * (a.gamma + 2) + a.gamma + 1];
         }
+        req[b] = o;
     }
 }
 
-// ================================================================= residual
-struct ResidArgs {
+// ===================================================================== draw
+struct DrawArgs {
     const char* target;
     const char* draft;
     int32_t* out_tokens;
@@ -518,124 +574,283 @@ struct ResidArgs {
     char* ws;
 };
 
-// Weight of element i of the draw: residual max(e_t - rho * e_d, 0) (both
-// relative to their rows' scales) or the target weight e_t.
-template <int ES>
-__device__ __forceinline__ float draw_weight(const ReqState& rs, const char* rt, const char* rd, int i,
-                                             float c_hi, float c_lo) {
-    const float et = scaled_exp(load_logit<ES>(rt, i), c_hi, c_lo, rs.M_t);
-    if (rs.mode != 1) return et;
-    const float ed = scaled_exp(load_logit<ES>(rd, i), c_hi, c_lo, rs.M_d);
-    return fmaxf(fmaf(-rs.rho_lo, ed, fmaf(-rs.rho_hi, ed, et)), 0.f);
-}
-
-template <int ES>
-__device__ __forceinline__ float weight_from_pair(const ReqState& rs, float zt, float zd, float c_hi,
-                                                  float c_lo) {
+// Weight of one element of the draw: the residual max(e_t - rho * e_d, 0)
+// (both relative to their rows' scales, rho = S_t / S_d as a float pair) or
+// the target weight e_t.  p_v - q_v = (e_t - rho * e_d) / S_t.
+__device__ __forceinline__ float draw_weight(const ReqState& rs, float zt, float zd, float c_hi,
+                                             float c_lo) {
     const float et = scaled_exp(zt, c_hi, c_lo, rs.M_t);
     if (rs.mode != 1) return et;
     const float ed = scaled_exp(zd, c_hi, c_lo, rs.M_d);
     return fmaxf(fmaf(-rs.rho_lo, ed, fmaf(-rs.rho_hi, ed, et)), 0.f);
 }
 
-// Sum of draw weights over chunk c of request b.
 template <int ES>
-__device__ float chunk_weight_sum(const ReqState& rs, const char* rt, const char* rd, int e0, int e1,
-                                  int lane, float c_hi, float c_lo) {
+__device__ __forceinline__ float draw_weight_at(const ReqState& rs, const char* rt, const char* rd, int i,
+                                                float c_hi, float c_lo) {
+    return draw_weight(rs, load_logit<ES>(rt, i), rs.mode == 1 ? load_logit<ES>(rd, i) : 0.f, c_hi, c_lo);
+}
+
+// Sum of the weights of one 16-byte vector pair.
+template <int ES>
+__device__ __forceinline__ float vec_weight_sum(const ReqState& rs, const uint4& t, const uint4& d, float c_hi,
+                                                float c_lo) {
+    const uint32_t tw[4] = {t.x, t.y, t.z, t.w}, dw[4] = {d.x, d.y, d.z, d.w};
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        if (ES == 2) {
+            s0 += draw_weight(rs, bf16_lo(tw[k]), bf16_lo(dw[k]), c_hi, c_lo);
+            s1 += draw_weight(rs, bf16_hi(tw[k]), bf16_hi(dw[k]), c_hi, c_lo);
+        } else {
+            s0 += draw_weight(rs, __uint_as_float(tw[k]), __uint_as_float(dw[k]), c_hi, c_lo);
+        }
+    }
+    return s0 + s1;
+}
+
+// Sum of the draw weights over elements [e0, e1) of the draw rows (one warp).
+template <int ES>
+__device__ float chunk_weight_sum(const ReqState& rs, const char* rt, const char* rd, int e0, int e1, int lane,
+                                  float c_hi, float c_lo) {
     constexpr int EPV = 16 / ES;
-    ChunkSpan st = chunk_span<ES>(rt, e0, e1);
+    constexpr int HALF = kVecPerLane / 2;
+    const ChunkSpan st = chunk_span<ES>(rt, e0, e1);
     bool vec = st.ia < st.ib;
     if (rs.mode == 1 && vec) {
         const ChunkSpan sd = chunk_span<ES>(rd, e0, e1);
         vec = sd.ia == st.ia && sd.ib == st.ib;  // same alignment in both rows
     }
-    float a0 = 0.f, a1 = 0.f;
+    float acc = 0.f;
     if (vec) {
-        const int nvec = (st.ib - st.ia) / EPV;
+        const int nvec = (st.ib - st.ia) / EPV;  // <= 32 * kVecPerLane
         const uint4* vt = (const uint4*)(rt + (size_t)st.ia * ES);
         const uint4* vd = (const uint4*)(rd + (size_t)st.ia * ES);
-        for (int i = lane; i < nvec; i += 32) {
-            const uint4 t = __ldg(vt + i);
-            uint4 d = make_uint4(0, 0, 0, 0);
-            if (rs.mode == 1) d = __ldg(vd + i);
-            if (ES == 2) {
-                const uint32_t tw[4] = {t.x, t.y, t.z, t.w}, dw[4] = {d.x, d.y, d.z, d.w};
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    a0 += weight_from_pair<ES>(rs, bf16_lo(tw[k]), bf16_lo(dw[k]), c_hi, c_lo);
-                    a1 += weight_from_pair<ES>(rs, bf16_hi(tw[k]), bf16_hi(dw[k]), c_hi, c_lo);
+        for (int h = 0; h < 2; ++h) {
+            uint4 tv[HALF], dv[HALF];
+#pragma unroll
+            for (int k = 0; k < HALF; ++k) {
+                const int i = lane + 32 * (h * HALF + k);
+                tv[k] = make_uint4(0, 0, 0, 0);
+                dv[k] = make_uint4(0, 0, 0, 0);
+                if (i < nvec) {
+                    tv[k] = __ldg(vt + i);
+                    if (rs.mode == 1) dv[k] = __ldg(vd + i);
                 }
-            } else {
-                a0 += weight_from_pair<ES>(rs, __uint_as_float(t.x), __uint_as_float(d.x), c_hi, c_lo);
-                a1 += weight_from_pair<ES>(rs, __uint_as_float(t.y), __uint_as_float(d.y), c_hi, c_lo);
-                a0 += weight_from_pair<ES>(rs, __uint_as_float(t.z), __uint_as_float(d.z), c_hi, c_lo);
-                a1 += weight_from_pair<ES>(rs, __uint_as_float(t.w), __uint_as_float(d.w), c_hi, c_lo);
             }
+#pragma unroll
+            for (int k = 0; k < HALF; ++k)
+                if (lane + 32 * (h * HALF + k) < nvec) acc += vec_weight_sum<ES>(rs, tv[k], dv[k], c_hi, c_lo);
         }
         const int si = span_scalar_index(st, lane);
-        if (si >= 0) a0 += draw_weight<ES>(rs, rt, rd, si, c_hi, c_lo);
+        if (si >= 0) acc += draw_weight_at<ES>(rs, rt, rd, si, c_hi, c_lo);
     } else {
-        for (int i = e0 + lane; i < e1; i += 32) a0 += draw_weight<ES>(rs, rt, rd, i, c_hi, c_lo);
+        for (int i = e0 + lane; i < e1; i += 32) acc += draw_weight_at<ES>(rs, rt, rd, i, c_hi, c_lo);
     }
-    return warp_sum(a0 + a1);
+    return warp_sum(acc);
 }
 
+// Inverse-CDF draw inside one chunk: the smallest element index whose running
+// weight (from 0 at the chunk start) exceeds r; if none, the last element with
+// positive weight (*no_bin set).  One warp.  Lane l owns a contiguous segment;
+// lane sums are fp32 (at most 64 terms), the prefix over lanes fp64; the
+// crossing segment is then re-read (L2) with its elements spread over the warp
+// for a second scan.
 template <int ES>
-__global__ void __launch_bounds__(256) k_resid_sum(ResidArgs a, Layout L) {
+__device__ int chunk_pick(const ReqState& rs, const char* rt, const char* rd, int e0, int e1, double r, int lane,
+                          float c_hi, float c_lo, bool* no_bin) {
+    constexpr int EPV = 16 / ES;
+    constexpr int SEG = kVecPerLane * EPV;  // elements per lane segment (64 bf16 / 32 fp32)
+    constexpr int EPL = SEG / 32;           // of those, per lane in the second scan
+    constexpr int HALF = kVecPerLane / 2;
+    const uint4* vt = (const uint4*)(rt + (size_t)e0 * ES);
+    const uint4* vd = (const uint4*)(rd + (size_t)e0 * ES);
+    // vector path: a full, 16-byte-aligned chunk; lane l owns vectors [8l, 8l+8)
+    const bool full = (e1 - e0) * ES == kChunkBytes && (((uintptr_t)vt & 15) == 0) &&
+                      (rs.mode != 1 || (((uintptr_t)vd & 15) == 0));
+    float lsum = 0.f;
+    int lpos = -1;
+    int s0, s1;
+    if (full) {
+        s0 = e0 + lane * SEG;
+        s1 = s0 + SEG;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint4 tv[HALF], dv[HALF];
+#pragma unroll
+            for (int k = 0; k < HALF; ++k) {
+                tv[k] = __ldcg(vt + lane * kVecPerLane + h * HALF + k);
+                dv[k] = rs.mode == 1 ? __ldcg(vd + lane * kVecPerLane + h * HALF + k) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int k = 0; k < HALF; ++k) {
+                const int base = s0 + (h * HALF + k) * EPV;
+                const uint32_t tw[4] = {tv[k].x, tv[k].y, tv[k].z, tv[k].w};
+                const uint32_t dw[4] = {dv[k].x, dv[k].y, dv[k].z, dv[k].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (ES == 2) {
+                        const float w0 = draw_weight(rs, bf16_lo(tw[q]), bf16_lo(dw[q]), c_hi, c_lo);
+                        const float w1 = draw_weight(rs, bf16_hi(tw[q]), bf16_hi(dw[q]), c_hi, c_lo);
+                        lsum += w0;
+                        if (w0 > 0.f) lpos = base + 2 * q;
+                        lsum += w1;
+                        if (w1 > 0.f) lpos = base + 2 * q + 1;
+                    } else {
+                        const float w0 =
+                            draw_weight(rs, __uint_as_float(tw[q]), __uint_as_float(dw[q]), c_hi, c_lo);
+                        lsum += w0;
+                        if (w0 > 0.f) lpos = base + q;
+                    }
+                }
+            }
+        }
+    } else {
+        const int seg = (e1 - e0 + 31) / 32;
+        s0 = min(e1, e0 + lane * seg);
+        s1 = min(e1, s0 + seg);
+        for (int i = s0; i < s1; ++i) {
+            const float w = draw_weight_at<ES>(rs, rt, rd, i, c_hi, c_lo);
+            lsum += w;
+            if (w > 0.f) lpos = i;
+        }
+    }
+    double excl = (double)lsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double t = __shfl_up_sync(0xffffffffu, excl, o);
+        if (lane >= o) excl += t;
+    }
+    excl -= (double)lsum;
+    const unsigned cross = __ballot_sync(0xffffffffu, s0 < s1 && excl + (double)lsum > r);
+    if (!cross) {
+        int lp = lpos;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
+        *no_bin = true;
+        return lp >= 0 ? lp : e1 - 1;
+    }
+    *no_bin = false;
+    const int l = __ffs(cross) - 1;
+    const float rr = (float)(r - __shfl_sync(0xffffffffu, excl, l));  // remainder inside segment l
+    const int seg0 = __shfl_sync(0xffffffffu, s0, l);
+    const int seg1 = __shfl_sync(0xffffffffu, s1, l);
+    const int segpos = __shfl_sync(0xffffffffu, lpos, l);
+    if (full) {
+        // lane i takes elements [i*EPL, (i+1)*EPL) of segment l
+        float w[EPL];
+        float part = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+            const int i = seg0 + lane * EPL + e;
+            w[e] = draw_weight_at<ES>(rs, rt, rd, i, c_hi, c_lo);
+            part += w[e];
+        }
+        float incl = part;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, incl > rr);
+        if (hit) {
+            const int i = __ffs(hit) - 1;
+            int v = -1;
+            if (lane == i) {
+                float cum = incl - part;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) {
+                    cum += w[e];
+                    if (v < 0 && cum > rr) v = e;
+                }
+                if (v < 0) v = EPL - 1;
+                v += seg0 + lane * EPL;
+            }
+            return __shfl_sync(0xffffffffu, v, i);
+        }
+        return segpos >= 0 ? segpos : seg1 - 1;
+    }
+    int v = -1;
+    if (lane == l) {
+        float cum = 0.f;
+        for (int i = s0; i < s1 && v < 0; ++i) {
+            cum += draw_weight_at<ES>(rs, rt, rd, i, c_hi, c_lo);
+            if (cum > rr) v = i;
+        }
+        if (v < 0) v = lpos >= 0 ? lpos : s1 - 1;
+    }
+    return __shfl_sync(0xffffffffu, v, l);
+}
+
+// Weight total of chunk c of the draw: the residual sums written by the draw
+// warps, or, for a bonus draw, the streaming kernel's chunk sums rescaled
+// exactly to the row scale.
+__device__ __forceinline__ float chunk_total(const ReqState& rs, const float* rchunk, const float2* tpart, int c) {
+    if (rs.mode == 1) return __ldcg(rchunk + c);
+    const float2 p = tpart[c];
+    if (p.x == -INFINITY) return 0.f;
+    const float d = p.x - rs.M_t;
+    return p.y * pow2_f(d < -1000.f ? -1000 : (int)d);
+}
+
+// One warp per (request, chunk): residual chunk sums.  The warp that completes
+// a request's last chunk (per-request ticket, zeroed by the accept kernel of
+// the same call) then draws the token: fp64 prefix over the chunk totals, then
+// chunk_pick inside the chosen chunk.  A bonus draw needs no pass over the row:
+// the warp of chunk 0 draws directly from the streaming kernel's chunk sums.
+constexpr int kDrawWarps = 8;
+
+template <int ES>
+__global__ void __launch_bounds__(kDrawWarps * 32, 4) k_draw(DrawArgs a, Layout L) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long long item = (long long)blockIdx.x * 8 + warp;
+    const long long item = (long long)blockIdx.x * kDrawWarps + warp;
+    pdl_wait();
     if (item >= (long long)a.B * L.nch) return;
     const int b = (int)(item / L.nch), c = (int)(item - (long long)b * L.nch);
-    const ReqState rs = ((const ReqState*)(a.ws + L.req))[b];
+    ReqState rs = ((const ReqState*)(a.ws + L.req))[b];
     if (rs.status != SPEC_OK || rs.mode == 0) return;
-    const int T1 = a.B * (a.gamma + 1);
-    const char* rt = a.target + (size_t)rs.g_t * a.V * ES;
-    const char* rd = rs.mode == 1 ? a.draft + (size_t)(rs.g_d - T1) * a.V * ES : rt;
-    const int e0 = c * L.CH, e1 = min(a.V, e0 + L.CH);
-    const float s = chunk_weight_sum<ES>(rs, rt, rd, e0, e1, lane, a.c_hi, a.c_lo);
-    if (lane == 0) ((float*)(a.ws + L.rchunk))[(size_t)b * L.nch + c] = s;
-}
-
-template <int ES>
-__global__ void __launch_bounds__(128) k_resid_pick(ResidArgs a, Layout L) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int b = blockIdx.x * 4 + warp;
-    if (b >= a.B) return;
-    ReqState* reqs = (ReqState*)(a.ws + L.req);
-    ReqState rs = reqs[b];
-    if (rs.status != SPEC_OK || rs.mode == 0) return;
+    if (rs.mode == 2 && c != 0) return;
     int* hdr = (int*)(a.ws + L.hdr);
     const int T1 = a.B * (a.gamma + 1);
     const char* rt = a.target + (size_t)rs.g_t * a.V * ES;
     const char* rd = rs.mode == 1 ? a.draft + (size_t)(rs.g_d - T1) * a.V * ES : rt;
     float* rchunk = (float*)(a.ws + L.rchunk) + (size_t)b * L.nch;
+    const float2* tpart = (const float2*)(a.ws + L.partial) + (size_t)rs.g_t * L.nch;
 
-    // total weight; an empty residual falls back to a draw from p of the same row
+    if (rs.mode == 1) {
+        const int e0 = c * L.CH, e1 = min(a.V, e0 + L.CH);
+        const float sum = chunk_weight_sum<ES>(rs, rt, rd, e0, e1, lane, a.c_hi, a.c_lo);
+        int last = 0;
+        if (lane == 0) {
+            rchunk[c] = sum;
+            __threadfence();
+            last = atomicAdd((int*)(a.ws + L.ticket) + b, 1) == L.nch - 1;
+        }
+        if (!__shfl_sync(0xffffffffu, last, 0)) return;
+        __threadfence();
+    }
+
+    // this warp draws the request's token
     double W = 0.0;
-    for (int c = lane; c < L.nch; c += 32) W += (double)rchunk[c];
+    for (int k = lane; k < L.nch; k += 32) W += (double)chunk_total(rs, rchunk, tpart, k);
     W = warp_sum_d(W);
     if (!(W > 0.0) && rs.mode == 1) {
+        // the residual summed to zero: draw from p of the same row instead
         rs.mode = 2;
+        rd = rt;
         if (lane == 0) atomicOr(&hdr[kHdrEvents], 1);
-        for (int c = 0; c < L.nch; ++c) {
-            const int e0 = c * L.CH, e1 = min(a.V, e0 + L.CH);
-            const float s = chunk_weight_sum<ES>(rs, rt, rt, e0, e1, lane, a.c_hi, a.c_lo);
-            if (lane == 0) rchunk[c] = s;
-        }
-        __syncwarp();
         W = 0.0;
-        for (int c = lane; c < L.nch; c += 32) W += (double)rchunk[c];
+        for (int k = lane; k < L.nch; k += 32) W += (double)chunk_total(rs, rchunk, tpart, k);
         W = warp_sum_d(W);
     }
     const double target = (double)rs.u * W;
-
-    // first chunk whose inclusive prefix exceeds u * W (fp64 prefix in chunk order)
-    int cstar = -1;
+    // first chunk whose inclusive fp64 prefix exceeds u * W
+    int cstar = -1, last_pos = -1;
     double before = 0.0, run = 0.0;
-    int last_pos = -1;
     for (int base = 0; base < L.nch && cstar < 0; base += 32) {
-        const int c = base + lane;
-        const double v = c < L.nch ? (double)rchunk[c] : 0.0;
+        const int k = base + lane;
+        const double v = k < L.nch ? (double)chunk_total(rs, rchunk, tpart, k) : 0.0;
         double incl = v;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -643,8 +858,8 @@ __global__ void __launch_bounds__(128) k_resid_pick(ResidArgs a, Layout L) {
             if (lane >= o) incl += t;
         }
         incl += run;
-        const unsigned hit = __ballot_sync(0xffffffffu, c < L.nch && incl > target);
-        const unsigned pos = __ballot_sync(0xffffffffu, c < L.nch && v > 0.0);
+        const unsigned hit = __ballot_sync(0xffffffffu, k < L.nch && incl > target);
+        const unsigned pos = __ballot_sync(0xffffffffu, k < L.nch && v > 0.0);
         if (pos) last_pos = base + 31 - __clz(pos);
         if (hit) {
             const int l = __ffs(hit) - 1;
@@ -657,52 +872,15 @@ __global__ void __launch_bounds__(128) k_resid_pick(ResidArgs a, Layout L) {
     if (cstar < 0) {  // rounding left no chunk: the last chunk with positive weight
         cstar = last_pos >= 0 ? last_pos : L.nch - 1;
         force_last = true;
-        before = 0.0;
     }
     const double r = force_last ? INFINITY : target - before;
-
-    // in-chunk scan: lane l owns a contiguous segment of the chunk
     const int e0 = cstar * L.CH, e1 = min(a.V, e0 + L.CH);
-    const int seg = (e1 - e0 + 31) / 32;
-    const int s0 = min(e1, e0 + lane * seg), s1 = min(e1, s0 + seg);
-    double lsum = 0.0;
-    int lpos = -1;
-    for (int i = s0; i < s1; ++i) {
-        const float w = draw_weight<ES>(rs, rt, rd, i, a.c_hi, a.c_lo);
-        lsum += (double)w;
-        if (w > 0.f) lpos = i;
-    }
-    double excl = lsum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const double t = __shfl_up_sync(0xffffffffu, excl, o);
-        if (lane >= o) excl += t;
-    }
-    excl -= lsum;
-    const unsigned cross = __ballot_sync(0xffffffffu, excl + lsum > r && s0 < s1);
-    int tok;
-    if (cross) {
-        const int l = __ffs(cross) - 1;
-        int v = -1;
-        if (lane == l) {
-            double cum = excl;
-            for (int i = s0; i < s1; ++i) {
-                cum += (double)draw_weight<ES>(rs, rt, rd, i, a.c_hi, a.c_lo);
-                if (cum > r) { v = i; break; }
-            }
-            if (v < 0) v = lpos >= 0 ? lpos : s1 - 1;
-        }
-        tok = __shfl_sync(0xffffffffu, v, l);
-    } else {
-        int lp = lpos;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
-        tok = lp >= 0 ? lp : e1 - 1;
-        if (lane == 0 && !force_last) atomicOr(&hdr[kHdrEvents], 2);
-    }
+    bool no_bin = false;
+    const int tok = chunk_pick<ES>(rs, rt, rd, e0, e1, r, lane, a.c_hi, a.c_lo, &no_bin);
     if (lane == 0) {
         a.out_tokens[(size_t)b * (a.gamma + 1) + rs.n] = tok;
         ((double*)(a.ws + L.mass))[b] = W / rs.S_t;
+        if (no_bin && !force_last) atomicOr(&hdr[kHdrEvents], 2);
     }
 }
 
@@ -750,7 +928,7 @@ int device_info(int& sms) {
         const void* fns[4] = {(const void*)k_row_stats<2, false>, (const void*)k_row_stats<2, true>,
                               (const void*)k_row_stats<4, false>, (const void*)k_row_stats<4, true>};
         for (const void* f : fns)
-            if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kStatsSmem) !=
+            if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStatsSmem) !=
                 cudaSuccess)
                 return SPEC_ERR_CUDA;
         d.attrs_set = true;
@@ -768,22 +946,31 @@ int check_shape(int B, int gamma, int V, spec_dtype dt) {
 }
 
 template <int ES, bool GREEDY>
-int launch_chain(const StatsArgs& sa, const AcceptArgs& aa, const ResidArgs& ra,
-                 const int32_t* verify_len, const int32_t* tokens, const float* uniforms,
-                 int32_t* out_tokens, int32_t* out_accept_len, const Layout& L, int sms,
+int launch_chain(const StatsArgs& sa, const AcceptArgs& aa, const DrawArgs& da, const Layout& L, int sms,
                  cudaStream_t st) {
-    k_plan<<<1, 1024, 0, st>>>(verify_len, tokens, uniforms, sa.B, sa.gamma, sa.V, GREEDY ? 1 : 0,
-                               out_tokens, out_accept_len, sa.ws, L);
     const long long max_items = (long long)L.R * L.nch;
     const int grid = (int)std::min<long long>(sms, (max_items + kStatsWarps - 1) / kStatsWarps);
     if (g_ev_before) cudaEventRecord(g_ev_before, st);
-    k_row_stats<ES, GREEDY><<<grid, kStatsWarps * 32, kStatsSmem, st>>>(sa, L);
+    k_row_stats<ES, GREEDY><<<grid, kStatsThreads, kStatsSmem, st>>>(sa, L);
     if (g_ev_after) cudaEventRecord(g_ev_after, st);
-    k_accept<ES, GREEDY><<<sa.B, 128, 0, st>>>(aa, L);
+    // the accept and draw kernels may be scheduled while their predecessor
+    // finishes; they wait for its results with griddepcontrol.wait
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)sa.B);
+    cfg.blockDim = dim3(kReqThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, k_accept<ES, GREEDY>, aa, L) != cudaSuccess) return SPEC_ERR_CUDA;
     if (!GREEDY) {
         const long long items = (long long)sa.B * L.nch;
-        k_resid_sum<ES><<<(unsigned)((items + 7) / 8), 256, 0, st>>>(ra, L);
-        k_resid_pick<ES><<<(sa.B + 3) / 4, 128, 0, st>>>(ra, L);
+        cfg.gridDim = dim3((unsigned)((items + kDrawWarps - 1) / kDrawWarps));
+        cfg.blockDim = dim3(kDrawWarps * 32);
+        if (cudaLaunchKernelEx(&cfg, k_draw<ES>, da, L) != cudaSuccess) return SPEC_ERR_CUDA;
     }
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
@@ -829,22 +1016,16 @@ int spec_verify(const void* target_logits, const void* draft_logits, spec_dtype 
     if ((double)c_hi >= c) c_hi = nextafterf(c_hi, 0.0f);
     const float c_lo = (float)(c - (double)c_hi);
 
-    StatsArgs sa{(const char*)target_logits, (const char*)draft_logits, B, gamma, V, c_hi, c_lo,
-                 (char*)workspace};
-    AcceptArgs aa{(const char*)target_logits, (const char*)draft_logits, draft_tokens, uniforms,
-                  out_tokens, out_accept_len, B, gamma, V, c_hi, c_lo, (char*)workspace};
-    ResidArgs ra{(const char*)target_logits, (const char*)draft_logits, out_tokens, B, gamma, V,
-                 c_hi, c_lo, (char*)workspace};
+    const char* t = (const char*)target_logits;
+    const char* d = (const char*)draft_logits;
+    char* ws = (char*)workspace;
+    StatsArgs sa{t, d, verify_len, B, gamma, V, c_hi, c_lo, ws};
+    AcceptArgs aa{t, d, draft_tokens, verify_len, uniforms, out_tokens, out_accept_len, B, gamma, V, c_hi, c_lo, ws};
+    DrawArgs da{t, d, out_tokens, B, gamma, V, c_hi, c_lo, ws};
     cudaStream_t st = (cudaStream_t)stream;
     if (es == 2)
-        return greedy ? launch_chain<2, true>(sa, aa, ra, verify_len, draft_tokens, uniforms, out_tokens,
-                                              out_accept_len, L, sms, st)
-                      : launch_chain<2, false>(sa, aa, ra, verify_len, draft_tokens, uniforms,
-                                               out_tokens, out_accept_len, L, sms, st);
-    return greedy ? launch_chain<4, true>(sa, aa, ra, verify_len, draft_tokens, uniforms, out_tokens,
-                                          out_accept_len, L, sms, st)
-                  : launch_chain<4, false>(sa, aa, ra, verify_len, draft_tokens, uniforms, out_tokens,
-                                           out_accept_len, L, sms, st);
+        return greedy ? launch_chain<2, true>(sa, aa, da, L, sms, st) : launch_chain<2, false>(sa, aa, da, L, sms, st);
+    return greedy ? launch_chain<4, true>(sa, aa, da, L, sms, st) : launch_chain<4, false>(sa, aa, da, L, sms, st);
 }
 
 int spec_verify_stats(const void* workspace, size_t workspace_bytes, int B, int gamma, int V,
@@ -870,7 +1051,7 @@ int spec_profile_events(void* before_row_stats, void* after_row_stats) {
 
 int spec_verify_kernel_count(int B, float temperature) {
     if (B <= 0) return 0;
-    return temperature == 0.0f ? 3 : 5;
+    return temperature == 0.0f ? 2 : 3;
 }
 
 }  // extern "C"
