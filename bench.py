@@ -33,7 +33,7 @@ METRIC = "verified rows/sec at B=64,γ=16,V=128k bf16; achieved HBM GB/s as % of
 UNIT = "verified rows/s"
 WORKLOAD = "block_diffusion"
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "row_stats_block_diffusion.md")
-KERNEL_SOURCES = ["speculative_decoding_verification_softmax_gb300/csrc/specv_verify.cu",
+KERNEL_SOURCES = ["speculative_decoding_verification_softmax_gb300/csrc/specv_rowstats.cuh",
                   "speculative_decoding_verification_softmax_gb300/csrc/specv_common.cuh"]
 
 

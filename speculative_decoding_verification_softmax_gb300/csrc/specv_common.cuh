@@ -16,7 +16,7 @@ namespace specv {
 constexpr int kChunkBytes = 4096;
 // Row-statistics kernel: warps per CTA and bulk-copy stages per warp.
 constexpr int kStatsWarps = 16;
-constexpr int kStages = 3;
+constexpr int kStages = 2;
 // Bound on any device wait (nanoseconds of %globaltimer).
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 

@@ -33,297 +33,13 @@
 #include <algorithm>
 #include <mutex>
 
-#include "specv_common.cuh"
+#include "specv_rowstats.cuh"
 
 namespace specv {
 
-// Descriptor of the chunk that occupies one ring stage.
-struct StageDesc {
-    ChunkSpan sp;
-    int g;  // global row id: target rows [0, B(gamma+1)), then draft rows
-    int c;  // chunk index within the row
-};
-
-constexpr int kStatsThreads = kStatsWarps * 32;
-constexpr size_t kRingBytes = (size_t)kStatsWarps * kStages * kChunkBytes;
-constexpr size_t kBarBytes = (size_t)kStatsWarps * kStages * 8;
-constexpr size_t kDescBytes = (size_t)kStatsWarps * kStages * sizeof(StageDesc);
-constexpr size_t kStatsSmem = kRingBytes + kBarBytes + kDescBytes + (SPEC_MAX_BATCH + 1) * 4 + 128;
-constexpr int kVecPerLane = kChunkBytes / 16 / 32;  // 16-byte vectors per lane in one chunk
-constexpr int kReqThreads = 512;                    // accept / draw kernels
+constexpr int kReqThreads = 512;  // accept / draw kernels
 
 __device__ __forceinline__ bool in01(float u) { return u >= 0.0f && u < 1.0f; }
-
-__device__ __forceinline__ double pow2_d(int e) {
-    return e < -1022 ? 0.0 : __longlong_as_double((long long)(1023 + e) << 52);
-}
-
-// Rows a request needs: target 0..ell and (T > 0) draft 0..ell-1; 0 when
-// verify_len is out of range (the accept kernel marks the request invalid).
-template <bool GREEDY>
-__device__ __forceinline__ int rows_of(const int32_t* verify_len, int b, int gamma) {
-    const int ell = verify_len ? verify_len[b] : gamma;
-    if (ell < 0 || ell > gamma) return 0;
-    return GREEDY ? ell + 1 : 2 * ell + 1;
-}
-
-// prefix[b] = sum of rows of requests < b, prefix[B] = total (whole CTA).
-template <bool GREEDY>
-__device__ void block_row_prefix(const int32_t* verify_len, int B, int gamma, int* prefix) {
-    __shared__ int s_w[32];
-    __shared__ int s_total;
-    constexpr int PER = (SPEC_MAX_BATCH + kStatsThreads - 1) / kStatsThreads;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    int cnt[PER];
-    int mine = 0;
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-        const int b = tid * PER + i;
-        cnt[i] = b < B ? rows_of<GREEDY>(verify_len, b, gamma) : 0;
-        mine += cnt[i];
-    }
-    int incl = mine;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-    }
-    if (lane == 31) s_w[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        const int w = lane < kStatsWarps ? s_w[lane] : 0;
-        int wi = w;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, wi, o);
-            if (lane >= o) wi += v;
-        }
-        s_w[lane] = wi - w;
-        if (lane == 31) s_total = wi;
-    }
-    __syncthreads();
-    int off = s_w[warp] + incl - mine;
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-        const int b = tid * PER + i;
-        if (b < B) prefix[b] = off;
-        off += cnt[i];
-    }
-    if (tid == 0) prefix[B] = s_total;
-}
-
-// ================================================================ row stats
-// Statistics of one chunk held in a ring stage (aligned interior) plus up to
-// 15 head / 7 tail elements loaded directly by lanes.
-template <int ES, bool GREEDY>
-__device__ __forceinline__ float2 chunk_stats(const char* stage, const ChunkSpan& sp, int lane,
-                                              float c_hi, float c_lo) {
-    constexpr int EPV = 16 / ES;  // elements per 16-byte vector
-    const int nvec = (sp.ib - sp.ia) / EPV;
-    const uint4* sm = (const uint4*)stage;
-    const int si = span_scalar_index(sp, lane);
-    const float sv = si >= 0 ? load_logit<ES>(sp.rowp, si) : -INFINITY;
-
-    // pass 1: max (NaN-propagating)
-    float m;
-    if (ES == 2) {
-        uint32_t pm = 0xFF80FF80u;  // (-inf, -inf)
-        int i = lane;
-        for (; i + 32 < nvec; i += 64) {
-            const uint4 x = sm[i], y = sm[i + 32];
-            pm = bf16x2_max_nan(pm, bf16x2_max_nan(bf16x2_max_nan(x.x, x.y), bf16x2_max_nan(x.z, x.w)));
-            pm = bf16x2_max_nan(pm, bf16x2_max_nan(bf16x2_max_nan(y.x, y.y), bf16x2_max_nan(y.z, y.w)));
-        }
-        if (i < nvec) {
-            const uint4 x = sm[i];
-            pm = bf16x2_max_nan(pm, bf16x2_max_nan(bf16x2_max_nan(x.x, x.y), bf16x2_max_nan(x.z, x.w)));
-        }
-        m = fmax_nan(bf16_lo(pm), bf16_hi(pm));
-    } else {
-        m = -INFINITY;
-        for (int i = lane; i < nvec; i += 32) {
-            const float4 x = ((const float4*)stage)[i];
-            m = fmax_nan(m, fmax_nan(fmax_nan(x.x, x.y), fmax_nan(x.z, x.w)));
-        }
-    }
-    m = fmax_nan(m, sv);
-    m = warp_max_nan(m);
-
-    if (GREEDY) {
-        // lowest index attaining the max
-        int best = 0x7fffffff;
-        if (!(m != m)) {
-            for (int i = lane; i < nvec && best == 0x7fffffff; i += 32) {
-                const int base = sp.ia + i * EPV;
-                if (ES == 2) {
-                    const uint4 x = sm[i];
-                    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        if (best == 0x7fffffff && bf16_lo(w[k]) == m) best = base + 2 * k;
-                        if (best == 0x7fffffff && bf16_hi(w[k]) == m) best = base + 2 * k + 1;
-                    }
-                } else {
-                    const float4 x = ((const float4*)stage)[i];
-                    const float w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        if (best == 0x7fffffff && w[k] == m) best = base + k;
-                }
-            }
-            if (si >= 0 && sv == m) best = min(best, si);
-        }
-        best = warp_min_i(best);
-        return make_float2(m, __int_as_float(best));
-    }
-
-    // T > 0: sum of 2^(z*c - Mc) with the integer scale Mc = ceil(max * c)
-    if (m != m || m == INFINITY) return make_float2(__int_as_float(0x7fc00000), 0.f);
-    if (m == -INFINITY) return make_float2(-INFINITY, 0.f);
-    const float Mc = ceilf(fmaf(m, c_hi, m * c_lo));
-    const float2 ch2 = make_float2(c_hi, c_hi), cl2 = make_float2(c_lo, c_lo), nm2 = make_float2(-Mc, -Mc);
-    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-    auto pair = [&](float z0, float z1) -> float2 {
-        const float2 z = make_float2(z0, z1);
-        const float2 t = __ffma2_rn(z, cl2, __ffma2_rn(z, ch2, nm2));
-        return make_float2(ex2_approx(t.x), ex2_approx(t.y));
-    };
-    if (ES == 2) {
-#pragma unroll 2
-        for (int i = lane; i < nvec; i += 32) {
-            const uint4 x = sm[i];
-            acc0 = __fadd2_rn(acc0, pair(bf16_lo(x.x), bf16_hi(x.x)));
-            acc1 = __fadd2_rn(acc1, pair(bf16_lo(x.y), bf16_hi(x.y)));
-            acc0 = __fadd2_rn(acc0, pair(bf16_lo(x.z), bf16_hi(x.z)));
-            acc1 = __fadd2_rn(acc1, pair(bf16_lo(x.w), bf16_hi(x.w)));
-        }
-    } else {
-#pragma unroll 2
-        for (int i = lane; i < nvec; i += 32) {
-            const float4 x = ((const float4*)stage)[i];
-            acc0 = __fadd2_rn(acc0, pair(x.x, x.y));
-            acc1 = __fadd2_rn(acc1, pair(x.z, x.w));
-        }
-    }
-    float S = (acc0.x + acc0.y) + (acc1.x + acc1.y);
-    if (si >= 0) S += scaled_exp(sv, c_hi, c_lo, Mc);
-    S = warp_sum(S);
-    return make_float2(Mc, S);
-}
-
-struct StatsArgs {
-    const char* target;
-    const char* draft;
-    const int32_t* verify_len;
-    int B, gamma, V;
-    float c_hi, c_lo;
-    char* ws;
-};
-
-template <int ES, bool GREEDY>
-__global__ void __launch_bounds__(kStatsThreads, 1) k_row_stats(StatsArgs a, Layout L) {
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 127) & ~uintptr_t(127));
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    unsigned char* ring = smem + (size_t)warp * kStages * kChunkBytes;
-    uint64_t* bars = (uint64_t*)(smem + kRingBytes) + warp * kStages;
-    StageDesc* desc = (StageDesc*)(smem + kRingBytes + kBarBytes) + warp * kStages;
-    int* prefix = (int*)(smem + kRingBytes + kBarBytes + kDescBytes);
-    int* hdr = (int*)(a.ws + L.hdr);
-    float2* partial = (float2*)(a.ws + L.partial);
-
-    if (blockIdx.x == 0 && tid == 0) {  // per-call reset of the status words
-        hdr[kHdrStatus] = 0;
-        hdr[kHdrEvents] = 0;
-    }
-    if (lane == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
-        fence_mbar_init();
-    }
-    block_row_prefix<GREEDY>(a.verify_len, a.B, a.gamma, prefix);
-    __syncthreads();
-    pdl_trigger();
-
-    const int nch = L.nch;
-    const long long total = (long long)prefix[a.B] * nch;
-    const int W = gridDim.x * kStatsWarps;
-    const int gw = blockIdx.x * kStatsWarps + warp;
-    if (gw >= total) return;
-    const long long count = (total - gw + W - 1) / W;  // items of this warp
-    const int Wq = W / nch, Wr = W - Wq * nch;
-    const int T1 = a.B * (a.gamma + 1);
-
-    // issue cursor (lane 0): compact row index, chunk, request of the row
-    int ir = gw / nch, ic = gw - (gw / nch) * nch, rb = 0;
-    auto issue = [&](int s) -> bool {
-        while (prefix[rb + 1] <= ir) ++rb;
-        const int k = ir - prefix[rb], cnt = prefix[rb + 1] - prefix[rb];
-        const int ell = GREEDY ? cnt - 1 : (cnt - 1) >> 1;
-        const int g = k <= ell ? rb * (a.gamma + 1) + k : T1 + rb * a.gamma + (k - ell - 1);
-        const char* rowp = g < T1 ? a.target + (size_t)g * a.V * ES
-                                  : a.draft + (size_t)(g - T1) * a.V * ES;
-        const int e0 = ic * L.CH;
-        StageDesc d;
-        d.sp = chunk_span<ES>(rowp, e0, min(a.V, e0 + L.CH));
-        d.g = g;
-        d.c = ic;
-        desc[s] = d;
-        const bool copy = d.sp.ia < d.sp.ib;
-        if (copy) {
-            const uint32_t bytes = (uint32_t)((d.sp.ib - d.sp.ia) * ES);
-            fence_proxy_async_smem();
-            mbar_arrive_expect_tx(&bars[s], bytes);
-            bulk_g2s(ring + (size_t)s * kChunkBytes, rowp + (size_t)d.sp.ia * ES, bytes, &bars[s]);
-        }
-        ic += Wr;
-        ir += Wq;
-        if (ic >= nch) {
-            ic -= nch;
-            ++ir;
-        }
-        return copy;
-    };
-
-    uint32_t pending = 0;  // bit s: a copy is in flight on stage s
-    uint32_t phase = 0;    // bit s: parity of the next wait on stage s
-    long long issued = 0;
-#pragma unroll 1
-    for (int s = 0; s < kStages && issued < count; ++s, ++issued) {
-        bool c = false;
-        if (lane == 0) c = issue(s);
-        if (__shfl_sync(0xffffffffu, c, 0)) pending |= 1u << s;
-    }
-    __syncwarp();
-
-    int s = 0;
-#pragma unroll 1
-    for (long long done = 0; done < count; ++done) {
-        const StageDesc d = desc[s];
-        if (pending & (1u << s)) {
-            if (!mbar_wait_bounded(&bars[s], (phase >> s) & 1u)) {
-                // record the failure and let this warp's copies in flight land
-                if (lane == 0) set_status(&hdr[kHdrStatus], SPEC_ERR_TIMEOUT);
-                for (int k = 0; k < kStages; ++k)
-                    if (k != s && (pending & (1u << k))) mbar_wait_bounded(&bars[k], (phase >> k) & 1u);
-                return;
-            }
-            phase ^= 1u << s;
-            pending &= ~(1u << s);
-        }
-        const float2 r = chunk_stats<ES, GREEDY>((const char*)(ring + (size_t)s * kChunkBytes), d.sp, lane,
-                                                 a.c_hi, a.c_lo);
-        if (lane == 0) partial[(size_t)d.g * nch + d.c] = r;
-        __syncwarp();
-        if (issued < count) {
-            bool c = false;
-            if (lane == 0) c = issue(s);
-            if (__shfl_sync(0xffffffffu, c, 0)) pending |= 1u << s;
-            ++issued;
-        }
-        __syncwarp();
-        s = (s + 1 == kStages) ? 0 : s + 1;
-    }
-}
 
 // =================================================================== accept
 struct AcceptArgs {
@@ -925,8 +641,11 @@ int device_info(int& sms) {
     if (!d.attrs_set) {
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return SPEC_ERR_CUDA;
-        const void* fns[4] = {(const void*)k_row_stats<2, false>, (const void*)k_row_stats<2, true>,
-                              (const void*)k_row_stats<4, false>, (const void*)k_row_stats<4, true>};
+        const void* fns[8] = {
+            (const void*)k_row_stats<2, false, false>, (const void*)k_row_stats<2, true, false>,
+            (const void*)k_row_stats<4, false, false>, (const void*)k_row_stats<4, true, false>,
+            (const void*)k_row_stats<2, false, true>,  (const void*)k_row_stats<2, true, true>,
+            (const void*)k_row_stats<4, false, true>,  (const void*)k_row_stats<4, true, true>};
         for (const void* f : fns)
             if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStatsSmem) !=
                 cudaSuccess)
@@ -947,11 +666,14 @@ int check_shape(int B, int gamma, int V, spec_dtype dt) {
 
 template <int ES, bool GREEDY>
 int launch_chain(const StatsArgs& sa, const AcceptArgs& aa, const DrawArgs& da, const Layout& L, int sms,
-                 cudaStream_t st) {
+                 bool aligned_rows, cudaStream_t st) {
     const long long max_items = (long long)L.R * L.nch;
     const int grid = (int)std::min<long long>(sms, (max_items + kStatsWarps - 1) / kStatsWarps);
     if (g_ev_before) cudaEventRecord(g_ev_before, st);
-    k_row_stats<ES, GREEDY><<<grid, kStatsThreads, kStatsSmem, st>>>(sa, L);
+    if (aligned_rows)
+        k_row_stats<ES, GREEDY, true><<<grid, kStatsThreads, kStatsSmem, st>>>(sa, L);
+    else
+        k_row_stats<ES, GREEDY, false><<<grid, kStatsThreads, kStatsSmem, st>>>(sa, L);
     if (g_ev_after) cudaEventRecord(g_ev_after, st);
     // the accept and draw kernels may be scheduled while their predecessor
     // finishes; they wait for its results with griddepcontrol.wait
@@ -1023,9 +745,14 @@ int spec_verify(const void* target_logits, const void* draft_logits, spec_dtype 
     AcceptArgs aa{t, d, draft_tokens, verify_len, uniforms, out_tokens, out_accept_len, B, gamma, V, c_hi, c_lo, ws};
     DrawArgs da{t, d, out_tokens, B, gamma, V, c_hi, c_lo, ws};
     cudaStream_t st = (cudaStream_t)stream;
+    // every row starts on a 16-byte boundary: whole-chunk copies
+    const bool al = aligned(target_logits, 16) && (greedy || gamma == 0 || aligned(draft_logits, 16)) &&
+                    ((size_t)V * es) % 16 == 0;
     if (es == 2)
-        return greedy ? launch_chain<2, true>(sa, aa, da, L, sms, st) : launch_chain<2, false>(sa, aa, da, L, sms, st);
-    return greedy ? launch_chain<4, true>(sa, aa, da, L, sms, st) : launch_chain<4, false>(sa, aa, da, L, sms, st);
+        return greedy ? launch_chain<2, true>(sa, aa, da, L, sms, al, st)
+                      : launch_chain<2, false>(sa, aa, da, L, sms, al, st);
+    return greedy ? launch_chain<4, true>(sa, aa, da, L, sms, al, st)
+                  : launch_chain<4, false>(sa, aa, da, L, sms, al, st);
 }
 
 int spec_verify_stats(const void* workspace, size_t workspace_bytes, int B, int gamma, int V,
