@@ -169,6 +169,42 @@ int spec_schedule(const float* confidence, int B, int gamma, const spec_cost_tab
                   int min_len, spec_sched_mode mode, int32_t* out_verify_len, void* workspace,
                   size_t workspace_bytes, spec_stream_t stream);
 
+/* ------------------------------------------------- verification, no workspace */
+
+/* Size of the device scratch array that spec_verify_static uses (8 MiB on each
+ * device that loads the library, held until the process exits). */
+#define SPEC_STATIC_WORKSPACE_BYTES (8u << 20)
+
+/*
+ * spec_verify without a workspace argument, for callers that cannot allocate
+ * device memory where they verify (an allocator that must not grow inside a
+ * capture or a latency-critical loop, a plugin handed only input and output
+ * buffers, a runtime with a memory budget fixed at start-up).  It has no
+ * counterpart on the pages: it is the same verification as spec_verify, with
+ * the scratch taken from a statically sized array in device memory instead
+ * of from the caller.
+ *
+ * Arguments, outputs and results are those of spec_verify.  It allocates
+ * nothing (no cudaMalloc, no cudaFree).
+ *   - Returns SPEC_ERR_WORKSPACE, launching nothing, when
+ *     spec_verify_workspace_bytes(B, gamma, V, dt) exceeds
+ *     SPEC_STATIC_WORKSPACE_BYTES (e.g. B=64, gamma=16, V=131072 bf16 needs
+ *     about 1.1 MiB; B=256, gamma=16, V=131072 about 4.3 MiB).
+ *   - The first call on a device looks up the array's device address with that
+ *     device current; make that first call before any stream capture.
+ *   - Every call on a device uses the same array and leaves its contents
+ *     behind.  Nothing in it needs to start at zero.  Calls that can overlap
+ *     on the GPU (different streams without ordering, or several host threads)
+ *     race on it: order them on one stream.
+ *   - The device status word lives in that array and cannot be read through
+ *     this call; invalid requests are still reported per request
+ *     (out_accept_len = -1).
+ */
+int spec_verify_static(const void* target_logits, const void* draft_logits, spec_dtype dt, int B, int gamma,
+                       int V, const int32_t* draft_tokens, const int32_t* verify_len, float temperature,
+                       const float* uniforms, int32_t* out_tokens, int32_t* out_accept_len,
+                       spec_stream_t stream);
+
 /* ------------------------------------------------------------------ status */
 
 /* Synchronises `stream`, reads the sticky device status word of `workspace`

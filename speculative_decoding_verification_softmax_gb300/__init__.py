@@ -18,7 +18,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _ROOT = os.path.dirname(_HERE)
 _CSRC = os.path.join(_HERE, "csrc")
 LIB_PATH = os.path.join(_HERE, "libspecv.so")
-SOURCES = ["specv_verify.cu", "specv_sched.cu", "specv_api.cu"]
+SOURCES = ["specv_verify.cu", "specv_sched.cu", "specv_api.cu", "specv_static.cu"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3", "-std=c++17",
               "-Xcompiler", "-fPIC", "-Xcompiler", "-O2"]
 
@@ -32,7 +32,9 @@ MAX_BATCH, MAX_GAMMA, MAX_SCHED_CANDIDATES = 4096, 32, 16384
 
 EXPORTED = ["spec_verify_workspace_bytes", "spec_verify", "spec_verify_stats",
             "spec_schedule_workspace_bytes", "spec_schedule", "spec_read_status",
-            "spec_status_string", "spec_profile_events", "spec_verify_kernel_count"]
+            "spec_status_string", "spec_profile_events", "spec_verify_kernel_count",
+            "spec_verify_static"]
+STATIC_WORKSPACE_BYTES = 8 << 20
 
 
 class SpecError(RuntimeError):
@@ -49,7 +51,8 @@ def _nvcc() -> str:
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile csrc/*.cu for sm_103a into libspecv.so (in-tree, parallel TUs)."""
     srcs = [os.path.join(_CSRC, s) for s in SOURCES]
-    deps = srcs + [os.path.join(_CSRC, "specv_common.cuh"), os.path.join(_ROOT, "include", "specv.h")]
+    deps = srcs + [os.path.join(_CSRC, "specv_common.cuh"), os.path.join(_CSRC, "specv_rowstats.cuh"),
+                   os.path.join(_ROOT, "include", "specv.h")]
     if (not force and os.path.exists(LIB_PATH)
             and all(os.path.getmtime(LIB_PATH) >= os.path.getmtime(d) for d in deps)):
         return LIB_PATH
@@ -111,6 +114,8 @@ def lib():
                 L.spec_profile_events.restype = i32
                 L.spec_verify_kernel_count.argtypes = [i32, f32]
                 L.spec_verify_kernel_count.restype = i32
+                L.spec_verify_static.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, f32, vp, vp, vp, vp]
+                L.spec_verify_static.restype = i32
                 _lib = L
     return _lib
 
@@ -213,6 +218,33 @@ def verify(target_logits, draft_logits, draft_tokens, verify_len, temperature: f
                            _stream_handle(stream))
     _check(rc, "spec_verify")
     return out_tokens, out_accept_len, workspace
+
+
+def verify_static(target_logits, draft_logits, draft_tokens, verify_len, temperature: float, uniforms,
+                  *, out_tokens=None, out_accept_len=None, stream=None):
+    """spec_verify_static: verification without a workspace, for callers that
+    cannot allocate device memory where they verify.  The scratch is a fixed
+    8 MiB array on the device (shared by all calls; order overlapping calls on
+    one stream).  Only the outputs, if not given, are allocated here.
+    Returns (out_tokens, out_accept_len)."""
+    torch = _torch()
+    B, G1, V = target_logits.shape
+    gamma = G1 - 1
+    dt = _dtype_code(target_logits)
+    dev = target_logits.device
+    for name, t in (("target_logits", target_logits), ("draft_logits", draft_logits),
+                    ("draft_tokens", draft_tokens), ("verify_len", verify_len), ("uniforms", uniforms)):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if out_tokens is None:
+        out_tokens = torch.empty((B, G1), dtype=torch.int32, device=dev)
+    if out_accept_len is None:
+        out_accept_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    rc = lib().spec_verify_static(_ptr(target_logits), _ptr(draft_logits), dt, B, gamma, V, _ptr(draft_tokens),
+                                  _ptr(verify_len), ctypes.c_float(temperature), _ptr(uniforms),
+                                  _ptr(out_tokens), _ptr(out_accept_len), _stream_handle(stream))
+    _check(rc, "spec_verify_static")
+    return out_tokens, out_accept_len
 
 
 def verify_stats(workspace, B: int, gamma: int, V: int, dtype_code: int, stream=None):
