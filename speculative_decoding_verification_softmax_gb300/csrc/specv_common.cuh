@@ -65,6 +65,33 @@ __device__ __forceinline__ DF warp_sum_df(DF v) {
     return v;
 }
 
+// a / b for two-float numbers (one correction step; about 44 significant bits).
+__device__ __forceinline__ DF df_div(DF a, DF b) {
+    const float q = a.hi / b.hi;
+    // remainder a - q * b, the product q * b.hi carried exactly by an fma
+    const float p = q * b.hi;
+    const float pe = fmaf(q, b.hi, -p);
+    const float rem = ((a.hi - p) - pe) + a.lo - q * b.lo;
+    DF r;
+    r.hi = q + rem / b.hi;
+    r.lo = (q - r.hi) + rem / b.hi;
+    return r;
+}
+
+// Inclusive warp scan of two-float values (lane order).
+__device__ __forceinline__ DF warp_scan_df(DF v, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        DF w;
+        w.hi = __shfl_up_sync(0xffffffffu, v.hi, o);
+        w.lo = __shfl_up_sync(0xffffffffu, v.lo, o);
+        if (lane >= o) v = df_add(w, v);
+    }
+    return v;
+}
+
+__device__ __forceinline__ double df_to_d(DF v) { return (double)v.hi + (double)v.lo; }
+
 // 2^e as a float for integer e <= 0 (0 below the normal range).
 __device__ __forceinline__ float pow2_f(int e) {
     return e < -126 ? 0.0f : __int_as_float((127 + e) << 23);
@@ -74,7 +101,7 @@ struct Layout {
     int R;        // B * (2*gamma + 1) potential rows
     int nch;      // chunks per row
     int CH;       // elements per chunk
-    size_t hdr, partial, req, pq, mass, rchunk, ticket, total;
+    size_t hdr, partial, req, pq, mass, rchunk, total;
 
     __host__ __device__ static size_t up(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -89,7 +116,6 @@ struct Layout {
         pq = o;       o = up(o + 2 * sizeof(double) * (size_t)B * (size_t)(gamma > 0 ? gamma : 1));
         mass = o;     o = up(o + sizeof(double) * (size_t)B);
         rchunk = o;   o = up(o + sizeof(float) * (size_t)B * (size_t)nch);
-        ticket = o;   o = up(o + sizeof(int) * (size_t)B);
         total = o;
     }
 };

@@ -55,8 +55,7 @@ extern "C" int spec_verify_static(const void* target_logits, const void* draft_l
     const int rc = static_workspace(&ws);
     if (rc != SPEC_OK) return rc;
     // Nothing in the scratch has to start at zero: every call writes each word
-    // it later reads (the kernels reset the status words and the completion
-    // tickets themselves).
+    // it later reads (the streaming kernel resets the status words itself).
     return spec_verify(target_logits, draft_logits, dt, B, gamma, V, draft_tokens, verify_len, temperature,
                        uniforms, out_tokens, out_accept_len, ws, SPEC_STATIC_WORKSPACE_BYTES, stream);
 }

@@ -20,40 +20,29 @@
 //                own ring of shared-memory stages filled by 1-D bulk copies
 //                (cp.async.bulk + mbarrier) and writes one partial per chunk:
 //                (integer scale, sum of 2^(z*c - scale)) or (max, argmax).
-//   k_accept     one CTA per request: validates the request, merges chunk
-//                partials per row (exact power-of-two rescaling, fp64 sums),
-//                computes p(x), q(x), runs the accept tests with one warp
-//                ballot, writes the accepted prefix and the draw job.
-//   k_draw       one warp per (request, chunk) (T > 0): weights of the 1-2
-//                draw rows summed per chunk; the warp finishing a request's
-//                last chunk takes the fp64 prefix over chunks and scans the
-//                chosen chunk for the inverse-CDF draw.
+//   k_finish     one thread-block cluster per request: validates the request,
+//                merges chunk partials per row (exact power-of-two rescaling,
+//                two-float sums), runs the accept tests with one warp ballot,
+//                writes the accepted prefix; at T > 0 sums the draw weights of
+//                the 1-2 draw rows per chunk across the cluster and draws the
+//                token by inverse CDF (fp64 prefix over chunk totals, then a
+//                scan inside the chosen chunk).
 #include <math.h>
 
 #include <algorithm>
 #include <mutex>
 
+#include <cooperative_groups.h>
+
 #include "specv_rowstats.cuh"
 
-namespace specv {
+namespace cg = cooperative_groups;
 
-constexpr int kReqThreads = 512;  // accept / draw kernels
+namespace specv {
 
 __device__ __forceinline__ bool in01(float u) { return u >= 0.0f && u < 1.0f; }
 
 // =================================================================== accept
-struct AcceptArgs {
-    const char* target;
-    const char* draft;
-    const int32_t* tokens;
-    const int32_t* verify_len;
-    const float* uniforms;
-    int32_t* out_tokens;
-    int32_t* out_accept_len;
-    int B, gamma, V;
-    float c_hi, c_lo;
-    char* ws;
-};
 
 // Merge the chunk partials of one row.  T > 0: M = max of the chunks'
 // integer scales, S = sum_c S_c * 2^(M_c - M) with exact power-of-two rescaling
@@ -117,178 +106,7 @@ __device__ __forceinline__ float div_df(float e, DF S) {
     return fmaf(-q, S.lo / S.hi, q);
 }
 
-template <int ES, bool GREEDY>
-__global__ void __launch_bounds__(kReqThreads) k_accept(AcceptArgs a, Layout L) {
-    constexpr int NW = kReqThreads / 32;
-    const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    __shared__ float s_M[2 * SPEC_MAX_GAMMA + 1];
-    __shared__ DF s_S[2 * SPEC_MAX_GAMMA + 1];
-    __shared__ int s_arg[2 * SPEC_MAX_GAMMA + 1];
-    __shared__ float s_zt[SPEC_MAX_GAMMA], s_zd[SPEC_MAX_GAMMA];
-    __shared__ int s_status;
-    int* hdr = (int*)(a.ws + L.hdr);
-    ReqState* req = (ReqState*)(a.ws + L.req);
-    const float2* partial = (const float2*)(a.ws + L.partial);
-    double* pq = (double*)(a.ws + L.pq);
-    const int G1 = a.gamma + 1, T1 = a.B * G1;
-    const int ell = a.verify_len ? a.verify_len[b] : a.gamma;
-    const bool ell_ok = ell >= 0 && ell <= a.gamma;
-
-    int st = SPEC_OK;
-    if (warp == 0) {
-        // caller inputs only (ready before the streaming kernel started):
-        // validation and the gathers of z at the (clamped) draft tokens
-        if (!ell_ok) st = SPEC_ERR_VERIFY_LEN;
-        const int j = lane;
-        int x = 0;
-        float uj = 0.f, ug = 0.f, ub = 0.f;
-        if (ell_ok && j < ell) x = a.tokens[(size_t)b * a.gamma + j];
-        if (!GREEDY && ell_ok) {
-            const float* u = a.uniforms + (size_t)b * (a.gamma + 2);
-            if (j < ell) uj = u[j];
-            if (j == 0) {
-                ug = u[a.gamma];
-                ub = u[a.gamma + 1];
-            }
-        }
-        const bool xok = x >= 0 && x < a.V;
-        if (!GREEDY && ell_ok && j < ell) {
-            const int xc = xok ? x : 0;
-            s_zt[j] = load_logit<ES>(a.target + (size_t)(b * G1 + j) * a.V * ES, xc);
-            s_zd[j] = load_logit<ES>(a.draft + (size_t)(b * a.gamma + j) * a.V * ES, xc);
-        }
-        if (st == SPEC_OK && !__all_sync(0xffffffffu, xok)) st = SPEC_ERR_TOKEN;
-        if (st == SPEC_OK && !GREEDY) {
-            bool uok = in01(uj);
-            if (j == 0) uok = uok && in01(ug) && in01(ub);
-            if (!__all_sync(0xffffffffu, uok)) st = SPEC_ERR_UNIFORM;
-        }
-    }
-    pdl_wait();  // the streaming kernel's partials and status word
-    pdl_trigger();
-    if (warp == 0) {
-        if (hdr[kHdrStatus] == SPEC_ERR_TIMEOUT) st = SPEC_ERR_TIMEOUT;
-        if (lane == 0) {
-            s_status = st;
-            ((int*)(a.ws + L.ticket))[b] = 0;  // completion ticket of the draw kernel
-        }
-    } else if (ell_ok) {
-        // row merges: target rows 0..ell, then draft rows 0..ell-1
-        const int nrows = GREEDY ? ell + 1 : 2 * ell + 1;
-        for (int r = warp - 1; r < nrows; r += NW - 1) {
-            const int g = r <= ell ? b * G1 + r : T1 + b * a.gamma + (r - ell - 1);
-            float M;
-            DF S;
-            int arg;
-            const bool ok = merge_row<GREEDY>(partial + (size_t)g * L.nch, L.nch, lane, M, S, arg);
-            if (lane == 0) {
-                s_M[r] = M;
-                s_S[r] = ok ? S : DF{__int_as_float(0x7fc00000), 0.f};  // NaN marks an invalid row
-                s_arg[r] = arg;
-            }
-        }
-    }
-    __syncthreads();
-    if (warp != 0) return;
-
-    st = s_status;
-    if (st == SPEC_OK) {
-        const int nrows = GREEDY ? ell + 1 : 2 * ell + 1;
-        bool bad = false;
-        for (int r = lane; r < nrows; r += 32) bad |= s_S[r].hi != s_S[r].hi;
-        if (__any_sync(0xffffffffu, bad)) st = SPEC_ERR_NONFINITE;
-    }
-    int32_t* ot = a.out_tokens + (size_t)b * G1;
-    const int j = lane;
-    if (st != SPEC_OK) {
-        for (int k = lane; k <= a.gamma; k += 32) ot[k] = -1;
-        for (int k = lane; k < a.gamma; k += 32) {
-            pq[2 * ((size_t)b * a.gamma + k)] = __longlong_as_double(0x7ff8000000000000ll);
-            pq[2 * ((size_t)b * a.gamma + k) + 1] = __longlong_as_double(0x7ff8000000000000ll);
-        }
-        if (lane == 0) {
-            a.out_accept_len[b] = -1;
-            ReqState o;
-            o.ell = 0;
-            o.status = st;
-            o.n = -1;
-            o.mode = 0;
-            req[b] = o;
-            ((double*)(a.ws + L.mass))[b] = __longlong_as_double(0x7ff8000000000000ll);
-            set_status(&hdr[kHdrStatus], st);
-        }
-        return;
-    }
-
-    // accept tests, one lane per position (gamma <= 32): u * q(x) < p(x)
-    const int32_t* x = a.tokens + (size_t)b * a.gamma;
-    bool acc = true;
-    double pxd = __longlong_as_double(0x7ff8000000000000ll), qxd = pxd;
-    if (j < ell) {
-        if (GREEDY) {
-            acc = x[j] == s_arg[j];
-        } else {
-            const float px = div_df(scaled_exp(s_zt[j], a.c_hi, a.c_lo, s_M[j]), s_S[j]);
-            const float qx = div_df(scaled_exp(s_zd[j], a.c_hi, a.c_lo, s_M[ell + 1 + j]), s_S[ell + 1 + j]);
-            const float u = a.uniforms[(size_t)b * (a.gamma + 2) + j];
-            acc = __fmul_rn(u, qx) < px;
-            pxd = px;
-            qxd = qx;
-        }
-    }
-    if (j < a.gamma) {
-        pq[2 * ((size_t)b * a.gamma + j)] = pxd;
-        pq[2 * ((size_t)b * a.gamma + j) + 1] = qxd;
-    }
-    const unsigned rej = __ballot_sync(0xffffffffu, !acc);
-    const int n = rej ? min(__ffs(rej) - 1, ell) : ell;
-    for (int k = lane; k <= a.gamma; k += 32) {
-        if (k < n) ot[k] = x[k];
-        else if (k > n) ot[k] = -1;
-    }
-    if (lane == 0) {
-        a.out_accept_len[b] = n;
-        ((double*)(a.ws + L.mass))[b] = __longlong_as_double(0x7ff8000000000000ll);
-        ReqState o;
-        o.ell = ell;
-        o.status = SPEC_OK;
-        o.n = n;
-        o.mode = 0;
-        o.g_t = b * G1 + n;
-        o.g_d = -1;
-        o.u = 0.f;
-        o.M_t = s_M[n];
-        o.M_d = 0.f;
-        o.rho_hi = o.rho_lo = 0.f;
-        o.pad = 0;
-        o.S_t = (double)s_S[n].hi + (double)s_S[n].lo;
-        if (GREEDY) {
-            ot[n] = s_arg[n];
-        } else if (n < ell) {
-            o.mode = 1;
-            o.g_d = T1 + b * a.gamma + n;
-            o.M_d = s_M[ell + 1 + n];
-            const double rho = o.S_t / ((double)s_S[ell + 1 + n].hi + (double)s_S[ell + 1 + n].lo);
-            o.rho_hi = (float)rho;
-            o.rho_lo = (float)(rho - (double)o.rho_hi);
-            o.u = a.uniforms[(size_t)b * (a.gamma + 2) + a.gamma];
-        } else {
-            o.mode = 2;
-            o.u = a.uniforms[(size_t)b * (a.gamma + 2) + a.gamma + 1];
-        }
-        req[b] = o;
-    }
-}
-
 // ===================================================================== draw
-struct DrawArgs {
-    const char* target;
-    const char* draft;
-    int32_t* out_tokens;
-    int B, gamma, V;
-    float c_hi, c_lo;
-    char* ws;
-};
 
 // Weight of one element of the draw: the residual max(e_t - rho * e_d, 0)
 // (both relative to their rows' scales, rho = S_t / S_d as a float pair) or
@@ -307,97 +125,70 @@ __device__ __forceinline__ float draw_weight_at(const ReqState& rs, const char* 
     return draw_weight(rs, load_logit<ES>(rt, i), rs.mode == 1 ? load_logit<ES>(rd, i) : 0.f, c_hi, c_lo);
 }
 
-// Sum of the weights of one 16-byte vector pair.
+// Sum of the weights of one 16-byte vector pair in element order.
 template <int ES>
-__device__ __forceinline__ float vec_weight_sum(const ReqState& rs, const uint4& t, const uint4& d, float c_hi,
-                                                float c_lo) {
+__device__ __forceinline__ float vec_weight_sum_ordered(const ReqState& rs, const uint4& t, const uint4& d,
+                                                        float c_hi, float c_lo) {
     const uint32_t tw[4] = {t.x, t.y, t.z, t.w}, dw[4] = {d.x, d.y, d.z, d.w};
-    float s0 = 0.f, s1 = 0.f;
+    float s = 0.f;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         if (ES == 2) {
-            s0 += draw_weight(rs, bf16_lo(tw[k]), bf16_lo(dw[k]), c_hi, c_lo);
-            s1 += draw_weight(rs, bf16_hi(tw[k]), bf16_hi(dw[k]), c_hi, c_lo);
+            s += draw_weight(rs, bf16_lo(tw[k]), bf16_lo(dw[k]), c_hi, c_lo);
+            s += draw_weight(rs, bf16_hi(tw[k]), bf16_hi(dw[k]), c_hi, c_lo);
         } else {
-            s0 += draw_weight(rs, __uint_as_float(tw[k]), __uint_as_float(dw[k]), c_hi, c_lo);
+            s += draw_weight(rs, __uint_as_float(tw[k]), __uint_as_float(dw[k]), c_hi, c_lo);
         }
     }
-    return s0 + s1;
+    return s;
 }
 
-// Sum of the draw weights over elements [e0, e1) of the draw rows (one warp).
+
+// Lane segments of a chunk [e0, e1): lane l owns a contiguous run of
+// elements.  A full, 16-byte-aligned chunk gives every lane kVecPerLane
+// vectors (64 bf16 / 32 fp32 elements); any other chunk is split evenly.
 template <int ES>
-__device__ float chunk_weight_sum(const ReqState& rs, const char* rt, const char* rd, int e0, int e1, int lane,
-                                  float c_hi, float c_lo) {
-    constexpr int EPV = 16 / ES;
-    constexpr int HALF = kVecPerLane / 2;
-    const ChunkSpan st = chunk_span<ES>(rt, e0, e1);
-    bool vec = st.ia < st.ib;
-    if (rs.mode == 1 && vec) {
-        const ChunkSpan sd = chunk_span<ES>(rd, e0, e1);
-        vec = sd.ia == st.ia && sd.ib == st.ib;  // same alignment in both rows
-    }
-    float acc = 0.f;
-    if (vec) {
-        const int nvec = (st.ib - st.ia) / EPV;  // <= 32 * kVecPerLane
-        const uint4* vt = (const uint4*)(rt + (size_t)st.ia * ES);
-        const uint4* vd = (const uint4*)(rd + (size_t)st.ia * ES);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            uint4 tv[HALF], dv[HALF];
-#pragma unroll
-            for (int k = 0; k < HALF; ++k) {
-                const int i = lane + 32 * (h * HALF + k);
-                tv[k] = make_uint4(0, 0, 0, 0);
-                dv[k] = make_uint4(0, 0, 0, 0);
-                if (i < nvec) {
-                    tv[k] = __ldg(vt + i);
-                    if (rs.mode == 1) dv[k] = __ldg(vd + i);
-                }
-            }
-#pragma unroll
-            for (int k = 0; k < HALF; ++k)
-                if (lane + 32 * (h * HALF + k) < nvec) acc += vec_weight_sum<ES>(rs, tv[k], dv[k], c_hi, c_lo);
-        }
-        const int si = span_scalar_index(st, lane);
-        if (si >= 0) acc += draw_weight_at<ES>(rs, rt, rd, si, c_hi, c_lo);
-    } else {
-        for (int i = e0 + lane; i < e1; i += 32) acc += draw_weight_at<ES>(rs, rt, rd, i, c_hi, c_lo);
-    }
-    return warp_sum(acc);
+__device__ __forceinline__ bool chunk_full(const ReqState& rs, const char* rt, const char* rd, int e0, int e1) {
+    return (e1 - e0) * ES == kChunkBytes && ((((uintptr_t)(rt + (size_t)e0 * ES)) & 15) == 0) &&
+           (rs.mode != 1 || ((((uintptr_t)(rd + (size_t)e0 * ES)) & 15) == 0));
 }
 
-// Inverse-CDF draw inside one chunk: the smallest element index whose running
-// weight (from 0 at the chunk start) exceeds r; if none, the last element with
-// positive weight (*no_bin set).  One warp.  Lane l owns a contiguous segment;
-// lane sums are fp32 (at most 64 terms), the prefix over lanes fp64; the
-// crossing segment is then re-read (L2) with its elements spread over the warp
-// for a second scan.
+// The chunk can be read as whole 16-byte vectors in both rows (always true
+// when the rows are 16-byte aligned and V * element size is a multiple of 16).
 template <int ES>
-__device__ int chunk_pick(const ReqState& rs, const char* rt, const char* rd, int e0, int e1, double r, int lane,
-                          float c_hi, float c_lo, bool* no_bin) {
+__device__ __forceinline__ bool chunk_vec(const ReqState& rs, const char* rt, const char* rd, int e0, int e1) {
+    return ((e1 - e0) * ES) % 16 == 0 && ((((uintptr_t)(rt + (size_t)e0 * ES)) & 15) == 0) &&
+           (rs.mode != 1 || ((((uintptr_t)(rd + (size_t)e0 * ES)) & 15) == 0));
+}
+
+template <int ES>
+__device__ __forceinline__ void seg_bounds(int e0, int e1, int lane, bool full, int& s0, int& s1) {
+    const int seg = full ? kVecPerLane * (16 / ES) : (e1 - e0 + 31) / 32;
+    s0 = min(e1, e0 + lane * seg);
+    s1 = min(e1, s0 + seg);
+}
+
+// fp32 sum (in element order) of the draw weights over this lane's segment,
+// and the last element with positive weight (-1 if none).
+template <int ES>
+__device__ __forceinline__ float seg_weight_sum(const ReqState& rs, const char* rt, const char* rd, int e0, int e1,
+                                                bool full, int lane, float c_hi, float c_lo, int& lpos) {
     constexpr int EPV = 16 / ES;
-    constexpr int SEG = kVecPerLane * EPV;  // elements per lane segment (64 bf16 / 32 fp32)
-    constexpr int EPL = SEG / 32;           // of those, per lane in the second scan
     constexpr int HALF = kVecPerLane / 2;
-    const uint4* vt = (const uint4*)(rt + (size_t)e0 * ES);
-    const uint4* vd = (const uint4*)(rd + (size_t)e0 * ES);
-    // vector path: a full, 16-byte-aligned chunk; lane l owns vectors [8l, 8l+8)
-    const bool full = (e1 - e0) * ES == kChunkBytes && (((uintptr_t)vt & 15) == 0) &&
-                      (rs.mode != 1 || (((uintptr_t)vd & 15) == 0));
-    float lsum = 0.f;
-    int lpos = -1;
     int s0, s1;
+    seg_bounds<ES>(e0, e1, lane, full, s0, s1);
+    float lsum = 0.f;
+    lpos = -1;
     if (full) {
-        s0 = e0 + lane * SEG;
-        s1 = s0 + SEG;
+        const uint4* vt = (const uint4*)(rt + (size_t)s0 * ES);
+        const uint4* vd = (const uint4*)(rd + (size_t)s0 * ES);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             uint4 tv[HALF], dv[HALF];
 #pragma unroll
             for (int k = 0; k < HALF; ++k) {
-                tv[k] = __ldcg(vt + lane * kVecPerLane + h * HALF + k);
-                dv[k] = rs.mode == 1 ? __ldcg(vd + lane * kVecPerLane + h * HALF + k) : make_uint4(0, 0, 0, 0);
+                tv[k] = __ldg(vt + h * HALF + k);
+                dv[k] = rs.mode == 1 ? __ldg(vd + h * HALF + k) : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
             for (int k = 0; k < HALF; ++k) {
@@ -423,180 +214,519 @@ __device__ int chunk_pick(const ReqState& rs, const char* rt, const char* rd, in
             }
         }
     } else {
-        const int seg = (e1 - e0 + 31) / 32;
-        s0 = min(e1, e0 + lane * seg);
-        s1 = min(e1, s0 + seg);
         for (int i = s0; i < s1; ++i) {
             const float w = draw_weight_at<ES>(rs, rt, rd, i, c_hi, c_lo);
             lsum += w;
             if (w > 0.f) lpos = i;
         }
     }
-    double excl = (double)lsum;
+    return lsum;
+}
+
+// The draw inside segment [seg0, seg1) (at most 64 elements) given the
+// remainder rr: its elements spread over the warp (one or two per lane), an
+// fp32 scan, the first element whose running weight exceeds rr; if rounding
+// leaves none, the segment's last element with positive weight.
+template <int ES>
+__device__ __forceinline__ int seg_pick(const ReqState& rs, const char* rt, const char* rd, int seg0, int seg1,
+                                        float rr, int lane, float c_hi, float c_lo) {
+    const int epl = (seg1 - seg0 + 31) / 32;
+    const int i0 = seg0 + lane * epl;
+    const float w0 = i0 < seg1 ? draw_weight_at<ES>(rs, rt, rd, i0, c_hi, c_lo) : 0.f;
+    const float w1 = (epl > 1 && i0 + 1 < seg1) ? draw_weight_at<ES>(rs, rt, rd, i0 + 1, c_hi, c_lo) : 0.f;
+    const float part = w0 + w1;
+    float incl = part;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const double t = __shfl_up_sync(0xffffffffu, excl, o);
-        if (lane >= o) excl += t;
+        const float t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
     }
-    excl -= (double)lsum;
-    const unsigned cross = __ballot_sync(0xffffffffu, s0 < s1 && excl + (double)lsum > r);
-    if (!cross) {
+    const unsigned hit = __ballot_sync(0xffffffffu, incl > rr);
+    if (hit) {
+        const int i = __ffs(hit) - 1;
+        const int v = ((incl - part) + w0 > rr || epl == 1) ? i0 : i0 + 1;
+        return __shfl_sync(0xffffffffu, v, i);
+    }
+    int lp = w1 > 0.f ? i0 + 1 : (w0 > 0.f ? i0 : -1);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
+    return lp >= 0 ? lp : seg1 - 1;
+}
+
+// A full, aligned chunk is 8 "rounds" of 32 consecutive 16-byte vectors; in
+// round k lane l holds vector 32k + l, so the rounds are contiguous runs of
+// elements and every load is coalesced.  Per-round weight sums over the warp:
+// lane l of the result holds the total of round l >> 2 (a transposing
+// butterfly: 9 shuffles for 8 sums).
+__device__ __forceinline__ float rounds_reduce(float (&v)[8], int lane) {
+    // step xor 16: lanes < 16 keep rounds 0-3, others 4-7
+    float a4[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float send = (lane & 16) ? v[k] : v[k + 4];
+        const float got = __shfl_xor_sync(0xffffffffu, send, 16);
+        a4[k] = ((lane & 16) ? v[k + 4] : v[k]) + got;
+    }
+    float a2[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const float send = (lane & 8) ? a4[k] : a4[k + 2];
+        const float got = __shfl_xor_sync(0xffffffffu, send, 8);
+        a2[k] = ((lane & 8) ? a4[k + 2] : a4[k]) + got;
+    }
+    const float send = (lane & 4) ? a2[0] : a2[1];
+    float a1 = ((lane & 4) ? a2[1] : a2[0]) + __shfl_xor_sync(0xffffffffu, send, 4);
+    a1 += __shfl_xor_sync(0xffffffffu, a1, 2);
+    a1 += __shfl_xor_sync(0xffffffffu, a1, 1);
+    return a1;
+}
+
+// Draw weights of a full chunk summed per round (fp32, element order inside a
+// lane's vector); returns this lane's share of the round totals (see above).
+// nvec: 16-byte vectors in the chunk (at most 256); vectors past it weigh 0.
+template <int ES>
+__device__ __forceinline__ float chunk_round_sums(const ReqState& rs, const char* rt, const char* rd, int e0,
+                                                  int nvec, int lane, float c_hi, float c_lo) {
+    constexpr int HALF = kVecPerLane / 2;
+    const uint4* vt = (const uint4*)(rt + (size_t)e0 * ES);
+    const uint4* vd = (const uint4*)(rd + (size_t)e0 * ES);
+    float r[8];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint4 tv[HALF], dv[HALF];
+#pragma unroll
+        for (int k = 0; k < HALF; ++k) {
+            const int i = 32 * (h * HALF + k) + lane;
+            tv[k] = make_uint4(0, 0, 0, 0);
+            dv[k] = make_uint4(0, 0, 0, 0);
+            if (i < nvec) {
+                tv[k] = __ldg(vt + i);
+                if (rs.mode == 1) dv[k] = __ldg(vd + i);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < HALF; ++k)
+            r[h * HALF + k] = 32 * (h * HALF + k) + lane < nvec
+                                  ? vec_weight_sum_ordered<ES>(rs, tv[k], dv[k], c_hi, c_lo) : 0.f;
+    }
+    return rounds_reduce(r, lane);
+}
+
+// The draw inside round k of a full chunk given the remainder rr: each lane
+// takes its vector (8 bf16 / 4 fp32 elements), fp32 lane sums, a warp scan,
+// then the crossing lane walks its elements; if rounding leaves no element,
+// the round's last element with positive weight.
+template <int ES>
+__device__ __forceinline__ int round_pick(const ReqState& rs, const char* rt, const char* rd, int e0, int nvec,
+                                          int k, float rr, int lane, float c_hi, float c_lo) {
+    constexpr int EPV = 16 / ES;
+    const bool in = 32 * k + lane < nvec;
+    const uint4 t = in ? __ldcg((const uint4*)(rt + (size_t)e0 * ES) + 32 * k + lane) : make_uint4(0, 0, 0, 0);
+    const uint4 d = (in && rs.mode == 1) ? __ldcg((const uint4*)(rd + (size_t)e0 * ES) + 32 * k + lane)
+                                         : make_uint4(0, 0, 0, 0);
+    const uint32_t tw[4] = {t.x, t.y, t.z, t.w}, dw[4] = {d.x, d.y, d.z, d.w};
+    float w[EPV];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        if (ES == 2) {
+            w[2 * q] = draw_weight(rs, bf16_lo(tw[q]), bf16_lo(dw[q]), c_hi, c_lo);
+            w[2 * q + 1] = draw_weight(rs, bf16_hi(tw[q]), bf16_hi(dw[q]), c_hi, c_lo);
+        } else {
+            w[q] = draw_weight(rs, __uint_as_float(tw[q]), __uint_as_float(dw[q]), c_hi, c_lo);
+        }
+    }
+    if (!in) {
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) w[e] = 0.f;
+    }
+    float ls = 0.f;
+    int lp = -1;
+    const int base = e0 + (32 * k + lane) * EPV;
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) {
+        ls += w[e];
+        if (w[e] > 0.f) lp = base + e;
+    }
+    float incl = ls;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, incl > rr);
+    if (hit) {
+        const int l = __ffs(hit) - 1;
+        int v = -1;
+        float cum = incl - ls;
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+            cum += w[e];
+            if (v < 0 && cum > rr) v = base + e;
+        }
+        if (v < 0) v = lp >= 0 ? lp : base + EPV - 1;
+        return __shfl_sync(0xffffffffu, v, l);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
+    return lp >= 0 ? lp : e0 + min(nvec, 32 * k + 32) * EPV - 1;
+}
+
+// First lane (or element) where an inclusive two-float scan of nonnegative
+// values exceeds the target; the exclusive prefix there.  Returns -1 if none.
+__device__ __forceinline__ int scan_find(DF v, DF target, int lane, DF& excl) {
+    const DF incl = warp_scan_df(v, lane);
+    const bool over = incl.hi > target.hi || (incl.hi == target.hi && incl.lo > target.lo);
+    const unsigned hit = __ballot_sync(0xffffffffu, over);
+    if (!hit) return -1;
+    const int l = __ffs(hit) - 1;
+    DF e = df_add(incl, DF{-v.hi, -v.lo});
+    excl.hi = __shfl_sync(0xffffffffu, e.hi, l);
+    excl.lo = __shfl_sync(0xffffffffu, e.lo, l);
+    return l;
+}
+
+// Inverse-CDF draw inside one chunk by a scan of its lane segments (one warp):
+// the smallest element index whose running weight (from 0 at the chunk start)
+// exceeds r; if none, the last element with positive weight.
+template <int ES>
+__device__ int chunk_pick(const ReqState& rs, const char* rt, const char* rd, int e0, int e1, DF r, int lane,
+                          float c_hi, float c_lo) {
+    const bool full = chunk_full<ES>(rs, rt, rd, e0, e1);
+    int lpos;
+    const float lsum = seg_weight_sum<ES>(rs, rt, rd, e0, e1, full, lane, c_hi, c_lo, lpos);
+    DF excl;
+    const int l = scan_find(DF{lsum, 0.f}, r, lane, excl);
+    if (l < 0) {
         int lp = lpos;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
-        *no_bin = true;
         return lp >= 0 ? lp : e1 - 1;
     }
-    *no_bin = false;
-    const int l = __ffs(cross) - 1;
-    const float rr = (float)(r - __shfl_sync(0xffffffffu, excl, l));  // remainder inside segment l
-    const int seg0 = __shfl_sync(0xffffffffu, s0, l);
-    const int seg1 = __shfl_sync(0xffffffffu, s1, l);
-    const int segpos = __shfl_sync(0xffffffffu, lpos, l);
-    if (full) {
-        // lane i takes elements [i*EPL, (i+1)*EPL) of segment l
-        float w[EPL];
-        float part = 0.f;
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) {
-            const int i = seg0 + lane * EPL + e;
-            w[e] = draw_weight_at<ES>(rs, rt, rd, i, c_hi, c_lo);
-            part += w[e];
-        }
-        float incl = part;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float t = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += t;
-        }
-        const unsigned hit = __ballot_sync(0xffffffffu, incl > rr);
-        if (hit) {
-            const int i = __ffs(hit) - 1;
-            int v = -1;
-            if (lane == i) {
-                float cum = incl - part;
-#pragma unroll
-                for (int e = 0; e < EPL; ++e) {
-                    cum += w[e];
-                    if (v < 0 && cum > rr) v = e;
-                }
-                if (v < 0) v = EPL - 1;
-                v += seg0 + lane * EPL;
-            }
-            return __shfl_sync(0xffffffffu, v, i);
-        }
-        return segpos >= 0 ? segpos : seg1 - 1;
-    }
-    int v = -1;
-    if (lane == l) {
-        float cum = 0.f;
-        for (int i = s0; i < s1 && v < 0; ++i) {
-            cum += draw_weight_at<ES>(rs, rt, rd, i, c_hi, c_lo);
-            if (cum > rr) v = i;
-        }
-        if (v < 0) v = lpos >= 0 ? lpos : s1 - 1;
-    }
-    return __shfl_sync(0xffffffffu, v, l);
+    int s0, s1;
+    seg_bounds<ES>(e0, e1, l, full, s0, s1);
+    const DF rem = df_add(r, DF{-excl.hi, -excl.lo});
+    return seg_pick<ES>(rs, rt, rd, s0, s1, rem.hi + rem.lo, lane, c_hi, c_lo);
 }
 
-// Weight total of chunk c of the draw: the residual sums written by the draw
-// warps, or, for a bonus draw, the streaming kernel's chunk sums rescaled
-// exactly to the row scale.
-__device__ __forceinline__ float chunk_total(const ReqState& rs, const float* rchunk, const float2* tpart, int c) {
-    if (rs.mode == 1) return __ldcg(rchunk + c);
-    const float2 p = tpart[c];
-    if (p.x == -INFINITY) return 0.f;
-    const float d = p.x - rs.M_t;
-    return p.y * pow2_f(d < -1000.f ? -1000 : (int)d);
-}
-
-// One warp per (request, chunk): residual chunk sums.  The warp that completes
-// a request's last chunk (per-request ticket, zeroed by the accept kernel of
-// the same call) then draws the token: fp64 prefix over the chunk totals, then
-// chunk_pick inside the chosen chunk.  A bonus draw needs no pass over the row:
-// the warp of chunk 0 draws directly from the streaming kernel's chunk sums.
-constexpr int kDrawWarps = 8;
-
+// The draw inside chunk [e0, e1) given the remainder r (one warp).  Whole-vector
+// chunks: the chunk's 8 round sums (given, or computed here with one coalesced
+// pass), a scan over them, then round_pick; other chunks: chunk_pick.
 template <int ES>
-__global__ void __launch_bounds__(kDrawWarps * 32, 4) k_draw(DrawArgs a, Layout L) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long long item = (long long)blockIdx.x * kDrawWarps + warp;
-    pdl_wait();
-    if (item >= (long long)a.B * L.nch) return;
-    const int b = (int)(item / L.nch), c = (int)(item - (long long)b * L.nch);
-    ReqState rs = ((const ReqState*)(a.ws + L.req))[b];
-    if (rs.status != SPEC_OK || rs.mode == 0) return;
-    if (rs.mode == 2 && c != 0) return;
-    int* hdr = (int*)(a.ws + L.hdr);
-    const int T1 = a.B * (a.gamma + 1);
-    const char* rt = a.target + (size_t)rs.g_t * a.V * ES;
-    const char* rd = rs.mode == 1 ? a.draft + (size_t)(rs.g_d - T1) * a.V * ES : rt;
-    float* rchunk = (float*)(a.ws + L.rchunk) + (size_t)b * L.nch;
-    const float2* tpart = (const float2*)(a.ws + L.partial) + (size_t)rs.g_t * L.nch;
-
-    if (rs.mode == 1) {
-        const int e0 = c * L.CH, e1 = min(a.V, e0 + L.CH);
-        const float sum = chunk_weight_sum<ES>(rs, rt, rd, e0, e1, lane, a.c_hi, a.c_lo);
-        int last = 0;
-        if (lane == 0) {
-            rchunk[c] = sum;
-            __threadfence();
-            last = atomicAdd((int*)(a.ws + L.ticket) + b, 1) == L.nch - 1;
-        }
-        if (!__shfl_sync(0xffffffffu, last, 0)) return;
-        __threadfence();
+__device__ int pick_in_chunk(const ReqState& rs, const char* rt, const char* rd, int e0, int e1, DF r,
+                             const float* rsum, int lane, float c_hi, float c_lo) {
+    if (!chunk_vec<ES>(rs, rt, rd, e0, e1)) return chunk_pick<ES>(rs, rt, rd, e0, e1, r, lane, c_hi, c_lo);
+    const int nvec = (e1 - e0) * ES / 16;
+    float rv;
+    if (rsum) {
+        rv = lane < 8 ? rsum[lane] : 0.f;
+    } else {
+        const float mine = chunk_round_sums<ES>(rs, rt, rd, e0, nvec, lane, c_hi, c_lo);
+        rv = __shfl_sync(0xffffffffu, mine, (lane & 7) * 4);
+        if (lane >= 8) rv = 0.f;
     }
+    DF excl;
+    const int k = scan_find(DF{rv, 0.f}, r, lane, excl);
+    if (k < 0) return chunk_pick<ES>(rs, rt, rd, e0, e1, DF{INFINITY, 0.f}, lane, c_hi, c_lo);
+    const DF rem = df_add(r, DF{-excl.hi, -excl.lo});
+    return round_pick<ES>(rs, rt, rd, e0, nvec, k, rem.hi + rem.lo, lane, c_hi, c_lo);
+}
 
-    // this warp draws the request's token
-    double W = 0.0;
-    for (int k = lane; k < L.nch; k += 32) W += (double)chunk_total(rs, rchunk, tpart, k);
-    W = warp_sum_d(W);
-    if (!(W > 0.0) && rs.mode == 1) {
+// ================================================================== finish
+// One thread-block cluster (cs CTAs of 16 warps) per request:
+//   1. (before the streaming kernel's results are needed) validation of the
+//      request's inputs and the gathers of z at the draft tokens, in every CTA;
+//   2. row merges spread over the cluster's warps, each merged row broadcast
+//      to every CTA's shared memory (distributed shared memory);
+//   3. cluster barrier; every CTA takes the same accept decision (one warp,
+//      one ballot); rank 0 writes the accepted prefix;
+//   4. T > 0 after a rejection: draw weights summed per chunk and per lane
+//      segment across the cluster's warps, written into rank 0's shared memory;
+//   5. cluster barrier; rank 0 draws the token by inverse CDF in three scans:
+//      chunk totals, the chosen chunk's lane-segment sums, the chosen
+//      segment's elements (two-float prefixes).  A bonus draw takes its chunk
+//      totals from the streaming kernel's partials and scans the chosen chunk.
+struct FinishArgs {
+    const char* target;
+    const char* draft;
+    const int32_t* tokens;
+    const int32_t* verify_len;
+    const float* uniforms;
+    int32_t* out_tokens;
+    int32_t* out_accept_len;
+    int B, gamma, V;
+    float c_hi, c_lo;
+    char* ws;
+};
+
+struct RowStatS {
+    float M;
+    DF S;  // NaN in S.hi marks an invalid row
+    int arg;
+};
+
+constexpr int kFinWarps = 16;
+constexpr int kFinThreads = kFinWarps * 32;
+constexpr int kMaxCluster = 4;
+constexpr int kChunkSmem = 2048;  // chunk totals kept in rank 0's shared memory
+constexpr int kRoundSmem = 1024;  // chunks whose round sums are kept there too
+
+// CTAs per request: enough warps for the rows to merge and the chunks to sum.
+inline int finish_cluster_size(int gamma, int nch, bool greedy) {
+    const int rows = greedy ? gamma + 1 : 2 * gamma + 1;
+    const int work = greedy ? rows : std::max(rows, nch);
+    return std::min(kMaxCluster, std::max(1, (work + kFinWarps - 1) / kFinWarps));
+}
+
+template <int ES, bool GREEDY>
+__global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout L) {
+    cg::cluster_group cluster = cg::this_cluster();
+    const int cs = (int)cluster.num_blocks();
+    const int rank = (int)cluster.block_rank();
+    const int b = blockIdx.x / cs;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gw = rank * kFinWarps + warp, nw = cs * kFinWarps;  // warp within the cluster
+    __shared__ RowStatS s_row[2 * SPEC_MAX_GAMMA + 1];
+    __shared__ float s_zt[SPEC_MAX_GAMMA], s_zd[SPEC_MAX_GAMMA];
+    __shared__ float s_ctot[kChunkSmem];
+    __shared__ float s_rsum[kRoundSmem][8];
+    __shared__ ReqState s_job;
+    int* hdr = (int*)(a.ws + L.hdr);
+    const float2* partial = (const float2*)(a.ws + L.partial);
+    const int G1 = a.gamma + 1, T1 = a.B * G1;
+    const int ell = a.verify_len ? a.verify_len[b] : a.gamma;
+    const bool ell_ok = ell >= 0 && ell <= a.gamma;
+
+    // 1. caller inputs only (ready before the streaming kernel started)
+    int st = SPEC_OK;
+    int x = 0;
+    float uj = 0.f, ug = 0.f, ub = 0.f;
+    if (warp == 0) {
+        if (!ell_ok) st = SPEC_ERR_VERIFY_LEN;
+        const int j = lane;
+        if (ell_ok && j < ell) x = a.tokens[(size_t)b * a.gamma + j];
+        if (!GREEDY && ell_ok) {
+            const float* u = a.uniforms + (size_t)b * (a.gamma + 2);
+            if (j < ell) uj = u[j];
+            ug = u[a.gamma];
+            ub = u[a.gamma + 1];
+        }
+        const bool xok = x >= 0 && x < a.V;
+        if (!GREEDY && ell_ok && j < ell) {
+            const int xc = xok ? x : 0;
+            s_zt[j] = load_logit<ES>(a.target + (size_t)(b * G1 + j) * a.V * ES, xc);
+            s_zd[j] = load_logit<ES>(a.draft + (size_t)(b * a.gamma + j) * a.V * ES, xc);
+        }
+        if (st == SPEC_OK && !__all_sync(0xffffffffu, xok)) st = SPEC_ERR_TOKEN;
+        if (st == SPEC_OK && !GREEDY) {
+            bool uok = in01(uj);
+            if (j == 0) uok = uok && in01(ug) && in01(ub);
+            if (!__all_sync(0xffffffffu, uok)) st = SPEC_ERR_UNIFORM;
+        }
+    }
+    pdl_wait();  // the streaming kernel's partials and status word
+    pdl_trigger();
+    const bool timed_out = warp == 0 && hdr[kHdrStatus] == SPEC_ERR_TIMEOUT;
+
+    // 2. row merges: target rows 0..ell, then draft rows 0..ell-1
+    const int nrows = ell_ok ? (GREEDY ? ell + 1 : 2 * ell + 1) : 0;
+    for (int r = gw; r < nrows; r += nw) {
+        const int g = r <= ell ? b * G1 + r : T1 + b * a.gamma + (r - ell - 1);
+        RowStatS rs;
+        const bool ok = merge_row<GREEDY>(partial + (size_t)g * L.nch, L.nch, lane, rs.M, rs.S, rs.arg);
+        if (!ok) rs.S = DF{__int_as_float(0x7fc00000), 0.f};
+        if (lane < cs) *cluster.map_shared_rank(&s_row[r], lane) = rs;  // to every CTA of the request
+    }
+    cluster.sync();
+
+    // 3. accept decision (identical in every CTA)
+    if (warp == 0) {
+        if (timed_out) st = SPEC_ERR_TIMEOUT;
+        if (st == SPEC_OK) {
+            bool bad = false;
+            for (int r = lane; r < nrows; r += 32) bad |= s_row[r].S.hi != s_row[r].S.hi;
+            if (__any_sync(0xffffffffu, bad)) st = SPEC_ERR_NONFINITE;
+        }
+        int32_t* ot = a.out_tokens + (size_t)b * G1;
+        double* pq = (double*)(a.ws + L.pq);
+        ReqState o;
+        o.ell = ell;
+        o.status = st;
+        o.n = -1;
+        o.mode = 0;
+        o.g_t = o.g_d = -1;
+        o.u = o.M_t = o.M_d = o.rho_hi = o.rho_lo = 0.f;
+        o.pad = 0;
+        o.S_t = 0.0;
+        if (st != SPEC_OK) {
+            if (rank == 0) {
+                for (int k = lane; k <= a.gamma; k += 32) ot[k] = -1;
+                for (int k = lane; k < a.gamma; k += 32) {
+                    pq[2 * ((size_t)b * a.gamma + k)] = __longlong_as_double(0x7ff8000000000000ll);
+                    pq[2 * ((size_t)b * a.gamma + k) + 1] = __longlong_as_double(0x7ff8000000000000ll);
+                }
+                if (lane == 0) {
+                    a.out_accept_len[b] = -1;
+                    ((double*)(a.ws + L.mass))[b] = __longlong_as_double(0x7ff8000000000000ll);
+                    set_status(&hdr[kHdrStatus], st);
+                }
+            }
+        } else {
+            // accept tests, one lane per position (gamma <= 32): u * q(x) < p(x)
+            const int j = lane;
+            bool acc = true;
+            float px = __int_as_float(0x7fc00000), qx = px;
+            if (j < ell) {
+                if (GREEDY) {
+                    acc = x == s_row[j].arg;
+                } else {
+                    px = div_df(scaled_exp(s_zt[j], a.c_hi, a.c_lo, s_row[j].M), s_row[j].S);
+                    qx = div_df(scaled_exp(s_zd[j], a.c_hi, a.c_lo, s_row[ell + 1 + j].M), s_row[ell + 1 + j].S);
+                    acc = __fmul_rn(uj, qx) < px;
+                }
+            }
+            const unsigned rej = __ballot_sync(0xffffffffu, !acc);
+            const int n = rej ? min(__ffs(rej) - 1, ell) : ell;
+            const DF St = s_row[n].S;
+            o.n = n;
+            o.g_t = b * G1 + n;
+            o.M_t = s_row[n].M;
+            o.S_t = df_to_d(St);
+            if (!GREEDY && n < ell) {
+                o.mode = 1;
+                o.g_d = T1 + b * a.gamma + n;
+                o.M_d = s_row[ell + 1 + n].M;
+                const DF rho = df_div(St, s_row[ell + 1 + n].S);
+                o.rho_hi = rho.hi;
+                o.rho_lo = rho.lo;
+                o.u = ug;
+            } else if (!GREEDY) {
+                o.mode = 2;
+                o.u = ub;
+            }
+            if (rank == 0) {
+                if (j < a.gamma) {
+                    pq[2 * ((size_t)b * a.gamma + j)] = (double)px;
+                    pq[2 * ((size_t)b * a.gamma + j) + 1] = (double)qx;
+                }
+                // lane k holds draft token k; slot gamma (32 at most) needs lane 0's help
+                if (lane < n) ot[lane] = x;
+                else if (lane > n && lane <= a.gamma) ot[lane] = -1;
+                if (lane == 0 && a.gamma == 32 && n < 32) ot[32] = -1;
+                if (lane == 0) {
+                    a.out_accept_len[b] = n;
+                    ((double*)(a.ws + L.mass))[b] = __longlong_as_double(0x7ff8000000000000ll);
+                    if (GREEDY) ot[n] = s_row[n].arg;
+                }
+            }
+        }
+        if (lane == 0) {
+            s_job = o;
+            if (rank == 0) ((ReqState*)(a.ws + L.req))[b] = o;
+        }
+    }
+    __syncthreads();
+    if (GREEDY) return;
+    ReqState job = s_job;
+    if (job.status != SPEC_OK) return;  // the same in every CTA of the cluster
+
+    // 4. residual sums per chunk and per lane segment over the cluster's warps
+    const char* rt = a.target + (size_t)job.g_t * a.V * ES;
+    const char* rd = job.mode == 1 ? a.draft + (size_t)(job.g_d - T1) * a.V * ES : rt;
+    float* rchunk = (float*)(a.ws + L.rchunk) + (size_t)b * L.nch;
+    const bool tot_smem = L.nch <= kChunkSmem;
+    const bool round_smem = L.nch <= kRoundSmem;
+    if (job.mode == 1) {
+        for (int c = gw; c < L.nch; c += nw) {
+            const int e0 = c * L.CH, e1 = min(a.V, e0 + L.CH);
+            float t;
+            if (chunk_vec<ES>(job, rt, rd, e0, e1)) {
+                // lane l holds the total of round l >> 2
+                const float rsum =
+                    chunk_round_sums<ES>(job, rt, rd, e0, (e1 - e0) * ES / 16, lane, a.c_hi, a.c_lo);
+                if (round_smem && (lane & 3) == 0) *cluster.map_shared_rank(&s_rsum[c][lane >> 2], 0) = rsum;
+                DF acc = {0.f, 0.f};
+#pragma unroll
+                for (int k = 0; k < 8; ++k) acc = df_add(acc, DF{__shfl_sync(0xffffffffu, rsum, 4 * k), 0.f});
+                t = acc.hi + acc.lo;
+            } else {
+                int lpos;
+                const float ls = seg_weight_sum<ES>(job, rt, rd, e0, e1, false, lane, a.c_hi, a.c_lo, lpos);
+                const DF tot = warp_sum_df(DF{ls, 0.f});
+                t = tot.hi + tot.lo;
+            }
+            if (lane == 0) {
+                if (tot_smem) *cluster.map_shared_rank(&s_ctot[c], 0) = t;
+                else rchunk[c] = t;
+            }
+        }
+        if (!tot_smem) __threadfence();
+    }
+    cluster.sync();
+    if (rank != 0 || warp != 0) return;
+
+    // 5. the draw (rank 0, warp 0)
+    const float2* tpart = partial + (size_t)job.g_t * L.nch;
+    auto total_of = [&](const ReqState& js, int c) -> float {
+        if (js.mode == 1) return tot_smem ? s_ctot[c] : __ldcg(rchunk + c);
+        const float2 p = tpart[c];
+        if (p.x == -INFINITY) return 0.f;
+        const float d = p.x - js.M_t;
+        return p.y * pow2_f(d < -1000.f ? -1000 : (int)d);
+    };
+    DF W = {0.f, 0.f};
+    for (int k = lane; k < L.nch; k += 32) W = df_add(W, DF{total_of(job, k), 0.f});
+    W = warp_sum_df(W);
+    if (!(W.hi > 0.f) && job.mode == 1) {
         // the residual summed to zero: draw from p of the same row instead
-        rs.mode = 2;
+        job.mode = 2;
         rd = rt;
         if (lane == 0) atomicOr(&hdr[kHdrEvents], 1);
-        W = 0.0;
-        for (int k = lane; k < L.nch; k += 32) W += (double)chunk_total(rs, rchunk, tpart, k);
-        W = warp_sum_d(W);
+        W = DF{0.f, 0.f};
+        for (int k = lane; k < L.nch; k += 32) W = df_add(W, DF{total_of(job, k), 0.f});
+        W = warp_sum_df(W);
     }
-    const double target = (double)rs.u * W;
-    // first chunk whose inclusive fp64 prefix exceeds u * W
+    // target = u * W as a two-float number
+    DF target;
+    {
+        const float p = job.u * W.hi;
+        const float pe = fmaf(job.u, W.hi, -p);
+        target = df_add(DF{p, 0.f}, DF{pe + job.u * W.lo, 0.f});
+    }
+    // level 1: chunk totals
     int cstar = -1, last_pos = -1;
-    double before = 0.0, run = 0.0;
+    DF before = {0.f, 0.f}, run = {0.f, 0.f};
     for (int base = 0; base < L.nch && cstar < 0; base += 32) {
         const int k = base + lane;
-        const double v = k < L.nch ? (double)chunk_total(rs, rchunk, tpart, k) : 0.0;
-        double incl = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const double t = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += t;
-        }
-        incl += run;
-        const unsigned hit = __ballot_sync(0xffffffffu, k < L.nch && incl > target);
-        const unsigned pos = __ballot_sync(0xffffffffu, k < L.nch && v > 0.0);
+        const float v = k < L.nch ? total_of(job, k) : 0.f;
+        DF excl;
+        const int l = scan_find(DF{v, 0.f}, df_add(target, DF{-run.hi, -run.lo}), lane, excl);
+        const unsigned pos = __ballot_sync(0xffffffffu, v > 0.f);
         if (pos) last_pos = base + 31 - __clz(pos);
-        if (hit) {
-            const int l = __ffs(hit) - 1;
+        if (l >= 0) {
             cstar = base + l;
-            before = __shfl_sync(0xffffffffu, incl - v, l);
+            before = df_add(run, excl);
+        } else {
+            DF blk = warp_sum_df(DF{v, 0.f});
+            run = df_add(run, blk);
         }
-        run = __shfl_sync(0xffffffffu, incl, 31);
     }
-    bool force_last = false;
-    if (cstar < 0) {  // rounding left no chunk: the last chunk with positive weight
+    int tok;
+    if (cstar < 0) {
+        // rounding left no chunk: the last element with positive weight of the
+        // last chunk with positive weight
         cstar = last_pos >= 0 ? last_pos : L.nch - 1;
-        force_last = true;
+        const int e0 = cstar * L.CH, e1 = min(a.V, e0 + L.CH);
+        tok = chunk_pick<ES>(job, rt, rd, e0, e1, DF{INFINITY, 0.f}, lane, a.c_hi, a.c_lo);
+        if (lane == 0) atomicOr(&hdr[kHdrEvents], 2);
+    } else {
+        const DF r = df_add(target, DF{-before.hi, -before.lo});
+        const int e0 = cstar * L.CH, e1 = min(a.V, e0 + L.CH);
+        const float* rsum = (job.mode == 1 && round_smem) ? s_rsum[cstar] : nullptr;
+        tok = pick_in_chunk<ES>(job, rt, rd, e0, e1, r, rsum, lane, a.c_hi, a.c_lo);
     }
-    const double r = force_last ? INFINITY : target - before;
-    const int e0 = cstar * L.CH, e1 = min(a.V, e0 + L.CH);
-    bool no_bin = false;
-    const int tok = chunk_pick<ES>(rs, rt, rd, e0, e1, r, lane, a.c_hi, a.c_lo, &no_bin);
     if (lane == 0) {
-        a.out_tokens[(size_t)b * (a.gamma + 1) + rs.n] = tok;
-        ((double*)(a.ws + L.mass))[b] = W / rs.S_t;
-        if (no_bin && !force_last) atomicOr(&hdr[kHdrEvents], 2);
+        a.out_tokens[(size_t)b * G1 + job.n] = tok;
+        ((double*)(a.ws + L.mass))[b] = df_to_d(W) / job.S_t;
     }
 }
 
@@ -665,8 +795,8 @@ int check_shape(int B, int gamma, int V, spec_dtype dt) {
 }
 
 template <int ES, bool GREEDY>
-int launch_chain(const StatsArgs& sa, const AcceptArgs& aa, const DrawArgs& da, const Layout& L, int sms,
-                 bool aligned_rows, cudaStream_t st) {
+int launch_chain(const StatsArgs& sa, const FinishArgs& fa, const Layout& L, int sms, bool aligned_rows,
+                 cudaStream_t st) {
     const long long max_items = (long long)L.R * L.nch;
     const int grid = (int)std::min<long long>(sms, (max_items + kStatsWarps - 1) / kStatsWarps);
     if (g_ev_before) cudaEventRecord(g_ev_before, st);
@@ -675,25 +805,24 @@ int launch_chain(const StatsArgs& sa, const AcceptArgs& aa, const DrawArgs& da, 
     else
         k_row_stats<ES, GREEDY, false><<<grid, kStatsThreads, kStatsSmem, st>>>(sa, L);
     if (g_ev_after) cudaEventRecord(g_ev_after, st);
-    // the accept and draw kernels may be scheduled while their predecessor
-    // finishes; they wait for its results with griddepcontrol.wait
-    cudaLaunchAttribute attr[1];
+    // one cluster per request; it may be scheduled while the streaming kernel
+    // finishes and waits for its results with griddepcontrol.wait
+    const int cs = finish_cluster_size(sa.gamma, L.nch, GREEDY);
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)cs;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)sa.B);
-    cfg.blockDim = dim3(kReqThreads);
+    cfg.gridDim = dim3((unsigned)(sa.B * cs));
+    cfg.blockDim = dim3(kFinThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, k_accept<ES, GREEDY>, aa, L) != cudaSuccess) return SPEC_ERR_CUDA;
-    if (!GREEDY) {
-        const long long items = (long long)sa.B * L.nch;
-        cfg.gridDim = dim3((unsigned)((items + kDrawWarps - 1) / kDrawWarps));
-        cfg.blockDim = dim3(kDrawWarps * 32);
-        if (cudaLaunchKernelEx(&cfg, k_draw<ES>, da, L) != cudaSuccess) return SPEC_ERR_CUDA;
-    }
+    cfg.numAttrs = 2;
+    if (cudaLaunchKernelEx(&cfg, k_finish<ES, GREEDY>, fa, L) != cudaSuccess) return SPEC_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
@@ -742,17 +871,14 @@ int spec_verify(const void* target_logits, const void* draft_logits, spec_dtype 
     const char* d = (const char*)draft_logits;
     char* ws = (char*)workspace;
     StatsArgs sa{t, d, verify_len, B, gamma, V, c_hi, c_lo, ws};
-    AcceptArgs aa{t, d, draft_tokens, verify_len, uniforms, out_tokens, out_accept_len, B, gamma, V, c_hi, c_lo, ws};
-    DrawArgs da{t, d, out_tokens, B, gamma, V, c_hi, c_lo, ws};
+    FinishArgs fa{t, d, draft_tokens, verify_len, uniforms, out_tokens, out_accept_len, B, gamma, V, c_hi, c_lo, ws};
     cudaStream_t st = (cudaStream_t)stream;
     // every row starts on a 16-byte boundary: whole-chunk copies
     const bool al = aligned(target_logits, 16) && (greedy || gamma == 0 || aligned(draft_logits, 16)) &&
                     ((size_t)V * es) % 16 == 0;
     if (es == 2)
-        return greedy ? launch_chain<2, true>(sa, aa, da, L, sms, al, st)
-                      : launch_chain<2, false>(sa, aa, da, L, sms, al, st);
-    return greedy ? launch_chain<4, true>(sa, aa, da, L, sms, al, st)
-                  : launch_chain<4, false>(sa, aa, da, L, sms, al, st);
+        return greedy ? launch_chain<2, true>(sa, fa, L, sms, al, st) : launch_chain<2, false>(sa, fa, L, sms, al, st);
+    return greedy ? launch_chain<4, true>(sa, fa, L, sms, al, st) : launch_chain<4, false>(sa, fa, L, sms, al, st);
 }
 
 int spec_verify_stats(const void* workspace, size_t workspace_bytes, int B, int gamma, int V,
@@ -778,7 +904,7 @@ int spec_profile_events(void* before_row_stats, void* after_row_stats) {
 
 int spec_verify_kernel_count(int B, float temperature) {
     if (B <= 0) return 0;
-    return temperature == 0.0f ? 2 : 3;
+    return 2;
 }
 
 }  // extern "C"

@@ -112,4 +112,4 @@ def test_status_strings(L):
 def test_kernel_count(L):
     assert sv.kernel_count(0, 1.0) == 0
     assert sv.kernel_count(4, 0.0) == 2
-    assert sv.kernel_count(4, 1.0) == 3
+    assert sv.kernel_count(4, 1.0) == 2
