@@ -127,6 +127,8 @@ def dist_env():
 
 
 def reduce_max(x: float, world: int, device) -> float:
+    """Max of x over all ranks (the slowest rank's time); device is where the
+    collective's tensor lives (cuda for NCCL, cpu for gloo)."""
     if world == 1:
         return x
     import torch

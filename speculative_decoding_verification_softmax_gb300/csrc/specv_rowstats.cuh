@@ -140,6 +140,59 @@ __device__ __forceinline__ float2 chunk_stats(const uint4* sm, int nvec_rt, int 
     constexpr int EPV = 16 / ES;  // elements per 16-byte vector
     const int nvec = NVEC > 0 ? NVEC : nvec_rt;  // NVEC > 0: a full chunk, loops unroll completely
 
+    if (GREEDY) {
+        // One pass: each lane's max and the first of its vectors attaining it
+        // (strict >, lanes walk their vectors in increasing index order).
+        float lm = -INFINITY;
+        int lv = lane;  // stays at the lane's first vector if all its values are -inf
+        bool nan = false;
+        for (int i = lane; i < nvec; i += 32) {
+            float vf;
+            if (ES == 2) {
+                const uint4 x = sm[i];
+                const uint32_t vm = bf16x2_max_nan(bf16x2_max_nan(x.x, x.y), bf16x2_max_nan(x.z, x.w));
+                vf = fmax_nan(bf16_lo(vm), bf16_hi(vm));
+            } else {
+                const float4 x = ((const float4*)sm)[i];
+                vf = fmax_nan(fmax_nan(x.x, x.y), fmax_nan(x.z, x.w));
+            }
+            nan |= vf != vf;
+            if (vf > lm) {
+                lm = vf;
+                lv = i;
+            }
+        }
+        if (si >= 0) nan |= sv != sv;
+        nan = __any_sync(0xffffffffu, nan);
+        float m = fmax_nan(lm, si >= 0 ? sv : -INFINITY);
+        m = nan ? __int_as_float(0x7fc00000) : warp_max_nan(m);
+        int best = 0x7fffffff;
+        if (!nan) {
+            if (lv < nvec && lm == m) {
+                // the lowest index equal to m inside the lane's first maximal vector
+                const int b0 = base + lv * EPV;
+                if (ES == 2) {
+                    const uint4 x = sm[lv];
+                    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                    for (int k = 3; k >= 0; --k) {
+                        if (bf16_hi(w[k]) == m) best = b0 + 2 * k + 1;
+                        if (bf16_lo(w[k]) == m) best = b0 + 2 * k;
+                    }
+                } else {
+                    const float4 x = ((const float4*)sm)[lv];
+                    const float w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                    for (int k = 3; k >= 0; --k)
+                        if (w[k] == m) best = b0 + k;
+                }
+            }
+            if (si >= 0 && sv == m) best = min(best, si);
+        }
+        best = warp_min_i(best);
+        return make_float2(m, __int_as_float(best));
+    }
+
     // pass 1: max (NaN-propagating)
     float m;
     if (ES == 2) {
@@ -164,34 +217,6 @@ __device__ __forceinline__ float2 chunk_stats(const uint4* sm, int nvec_rt, int 
     }
     if (si >= 0) m = fmax_nan(m, sv);
     m = warp_max_nan(m);
-
-    if (GREEDY) {
-        // lowest index attaining the max
-        int best = 0x7fffffff;
-        if (!(m != m)) {
-            for (int i = lane; i < nvec && best == 0x7fffffff; i += 32) {
-                const int b0 = base + i * EPV;
-                if (ES == 2) {
-                    const uint4 x = sm[i];
-                    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        if (best == 0x7fffffff && bf16_lo(w[k]) == m) best = b0 + 2 * k;
-                        if (best == 0x7fffffff && bf16_hi(w[k]) == m) best = b0 + 2 * k + 1;
-                    }
-                } else {
-                    const float4 x = ((const float4*)sm)[i];
-                    const float w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        if (best == 0x7fffffff && w[k] == m) best = b0 + k;
-                }
-            }
-            if (si >= 0 && sv == m) best = min(best, si);
-        }
-        best = warp_min_i(best);
-        return make_float2(m, __int_as_float(best));
-    }
 
     // T > 0: sum of 2^(z*c - Mc) with the integer scale Mc = ceil(max * c)
     if (m != m || m == INFINITY) return make_float2(__int_as_float(0x7fc00000), 0.f);
