@@ -15,7 +15,7 @@ namespace specv {
 // and of the residual pass.  4 KiB = 2048 bf16 or 1024 fp32 logits.
 constexpr int kChunkBytes = 4096;
 // Row-statistics kernel: warps per CTA and bulk-copy stages per warp.
-constexpr int kStatsWarps = 16;
+constexpr int kStatsWarps = 20;
 constexpr int kStages = 2;
 // Bound on any device wait (nanoseconds of %globaltimer).
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;

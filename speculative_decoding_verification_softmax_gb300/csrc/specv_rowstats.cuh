@@ -10,7 +10,7 @@
 // argmax.  The accept kernel merges the chunks of a row exactly (power-of-two
 // rescaling).
 //
-// Layout: a persistent grid, one CTA per SM, 16 warps.  Each warp owns a ring
+// Layout: a persistent grid, one CTA per SM, 20 warps.  Each warp owns a ring
 // of kStages shared-memory stages that it fills itself with 1-D bulk copies
 // (cp.async.bulk, completion on an mbarrier) and consumes in order; no
 // cross-warp synchronisation.  Work items (compact row, chunk) are dealt to
@@ -38,7 +38,7 @@ struct StageDesc {
 };
 
 constexpr int kStatsThreads = kStatsWarps * 32;
-constexpr int kTableRows = 16384;  // compact rows listed in shared memory
+constexpr int kTableRows = 4096;  // compact rows listed in shared memory (more: prefix walk)
 constexpr size_t kRingBytes = (size_t)kStatsWarps * kStages * kChunkBytes;
 constexpr size_t kBarBytes = (size_t)kStatsWarps * kStages * 8;
 constexpr size_t kDescBytes = (size_t)kStatsWarps * kStages * sizeof(StageDesc);
@@ -222,33 +222,32 @@ __device__ __forceinline__ float2 chunk_stats(const uint4* sm, int nvec_rt, int 
     if (m != m || m == INFINITY) return make_float2(__int_as_float(0x7fc00000), 0.f);
     if (m == -INFINITY) return make_float2(-INFINITY, 0.f);
     const float Mc = ceilf(fmaf(m, c_hi, m * c_lo));
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    // packed FP32x2 arithmetic: (z*c_hi - Mc) + z*c_lo for two elements per FMA
+    const float2 ch2 = make_float2(c_hi, c_hi), cl2 = make_float2(c_lo, c_lo), nm2 = make_float2(-Mc, -Mc);
+    float2 p0 = make_float2(0.f, 0.f), p1 = p0;
+    auto pair = [&](float z0, float z1) -> float2 {
+        const float2 z = make_float2(z0, z1);
+        const float2 t = __ffma2_rn(z, cl2, __ffma2_rn(z, ch2, nm2));
+        return make_float2(ex2_approx(t.x), ex2_approx(t.y));
+    };
     if (ES == 2) {
 #pragma unroll 4
         for (int i = lane; i < nvec; i += 32) {
             const uint4 x = sm[i];
-            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                if (k & 1) {
-                    a2 += scaled_exp(bf16_lo(w[k]), c_hi, c_lo, Mc);
-                    a3 += scaled_exp(bf16_hi(w[k]), c_hi, c_lo, Mc);
-                } else {
-                    a0 += scaled_exp(bf16_lo(w[k]), c_hi, c_lo, Mc);
-                    a1 += scaled_exp(bf16_hi(w[k]), c_hi, c_lo, Mc);
-                }
-            }
+            p0 = __fadd2_rn(p0, pair(bf16_lo(x.x), bf16_hi(x.x)));
+            p1 = __fadd2_rn(p1, pair(bf16_lo(x.y), bf16_hi(x.y)));
+            p0 = __fadd2_rn(p0, pair(bf16_lo(x.z), bf16_hi(x.z)));
+            p1 = __fadd2_rn(p1, pair(bf16_lo(x.w), bf16_hi(x.w)));
         }
     } else {
-#pragma unroll 2
+#pragma unroll 4
         for (int i = lane; i < nvec; i += 32) {
             const float4 x = ((const float4*)sm)[i];
-            a0 += scaled_exp(x.x, c_hi, c_lo, Mc);
-            a1 += scaled_exp(x.y, c_hi, c_lo, Mc);
-            a2 += scaled_exp(x.z, c_hi, c_lo, Mc);
-            a3 += scaled_exp(x.w, c_hi, c_lo, Mc);
+            p0 = __fadd2_rn(p0, pair(x.x, x.y));
+            p1 = __fadd2_rn(p1, pair(x.z, x.w));
         }
     }
+    float a0 = p0.x, a1 = p0.y, a2 = p1.x, a3 = p1.y;
     if (si >= 0) a0 += scaled_exp(sv, c_hi, c_lo, Mc);
     return make_float2(Mc, warp_sum((a0 + a1) + (a2 + a3)));
 }
