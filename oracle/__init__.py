@@ -53,8 +53,14 @@ def _L():
         lib.oracle_sched_exact.argtypes = [vp, i32, i32, vp, vp, i32, i32, vp, vp, vp]
         lib.oracle_sched_alg1.argtypes = [vp, i32, i32, vp, vp, i32, i32, vp]
         lib.oracle_sched_brute.argtypes = [vp, i32, i32, vp, vp, i32, i32, vp, vp, vp]
+        lib.oracle_set_sts.argtypes = [vp]
+        lib.oracle_sched_dcut.argtypes = [vp, i32, i32, vp, vp, i32, i32, vp, vp]
+        lib.oracle_sched_threshold.argtypes = [vp, i32, i32, dbl, i32, vp]
+        lib.oracle_sts_ece.argtypes = [vp, vp, i32, i32, vp]
+        lib.oracle_sts_fit.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp]
         for f in ("oracle_verify", "oracle_verify_probs", "oracle_cost_at", "oracle_sched_exact",
-                  "oracle_sched_alg1", "oracle_sched_brute"):
+                  "oracle_sched_alg1", "oracle_sched_brute", "oracle_set_sts", "oracle_sched_dcut",
+                  "oracle_sched_threshold", "oracle_sts_ece", "oracle_sts_fit"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -127,7 +133,18 @@ def cost_at(N: float, cost) -> float:
     return r.value
 
 
-def _sched(fn, conf, cost, min_len, with_obj=True):
+_sts_keep = None
+
+
+def _set_sts(sts_T):
+    """Calibration temperatures for the next scheduler call (None: none)."""
+    global _sts_keep
+    _sts_keep = None if sts_T is None else np.ascontiguousarray(sts_T, np.float64)
+    _L().oracle_set_sts(_p(_sts_keep))
+
+
+def _sched(fn, conf, cost, min_len, with_obj=True, sts_T=None):
+    _set_sts(sts_T)
     conf = np.ascontiguousarray(conf, np.float32)
     B, gamma = conf.shape
     kt, kc = _knots(cost)
@@ -141,13 +158,55 @@ def _sched(fn, conf, cost, min_len, with_obj=True):
     return dict(rc=rc, verify_len=out)
 
 
-def sched_exact(conf, cost, min_len: int = 0) -> dict:
-    return _sched(_L().oracle_sched_exact, conf, cost, min_len)
+def sched_exact(conf, cost, min_len: int = 0, sts_T=None) -> dict:
+    return _sched(_L().oracle_sched_exact, conf, cost, min_len, sts_T=sts_T)
 
 
-def sched_alg1(conf, cost, min_len: int = 0) -> dict:
-    return _sched(_L().oracle_sched_alg1, conf, cost, min_len, with_obj=False)
+def sched_alg1(conf, cost, min_len: int = 0, sts_T=None) -> dict:
+    return _sched(_L().oracle_sched_alg1, conf, cost, min_len, with_obj=False, sts_T=sts_T)
 
 
-def sched_brute(conf, cost, min_len: int = 0) -> dict:
-    return _sched(_L().oracle_sched_brute, conf, cost, min_len)
+def sched_brute(conf, cost, min_len: int = 0, sts_T=None) -> dict:
+    return _sched(_L().oracle_sched_brute, conf, cost, min_len, sts_T=sts_T)
+
+
+def sched_dcut(conf, ratios, costs, min_len: int = 0, sts_T=None) -> dict:
+    """D-cut: the best of the budgets ceil(rho * B(gamma+1)) by progress / cost."""
+    _set_sts(sts_T)
+    conf = np.ascontiguousarray(conf, np.float32)
+    B, gamma = conf.shape
+    r = np.ascontiguousarray(ratios, np.float64)
+    c = np.ascontiguousarray(costs, np.float64)
+    out = np.full(B, -1, np.int32)
+    choice = ctypes.c_int(-1)
+    rc = _L().oracle_sched_dcut(_p(conf), B, gamma, _p(r), _p(c), len(r), min_len, _p(out), ctypes.byref(choice))
+    return dict(rc=rc, verify_len=out, choice=choice.value)
+
+
+def sched_threshold(conf, threshold: float, min_len: int = 0, sts_T=None) -> dict:
+    _set_sts(sts_T)
+    conf = np.ascontiguousarray(conf, np.float32)
+    B, gamma = conf.shape
+    out = np.full(B, -1, np.int32)
+    rc = _L().oracle_sched_threshold(_p(conf), B, gamma, float(threshold), min_len, _p(out))
+    return dict(rc=rc, verify_len=out)
+
+
+def sts_ece(a, y, bins: int = 15) -> float:
+    a = np.ascontiguousarray(a, np.float64)
+    y = np.ascontiguousarray(y, np.int32)
+    out = ctypes.c_double()
+    _L().oracle_sts_ece(_p(a), _p(y), len(a), bins, ctypes.byref(out))
+    return out.value
+
+
+def sts_fit(conf, accept_len, grid: int = 100, bins: int = 15) -> dict:
+    """STS temperatures (one per position) from confidences [n, gamma] and the
+    accept lengths observed when verifying all gamma positions."""
+    conf = np.ascontiguousarray(conf, np.float32)
+    n, gamma = conf.shape
+    al = np.ascontiguousarray(accept_len, np.int32)
+    T = np.empty(gamma)
+    e = np.empty(gamma)
+    rc = _L().oracle_sts_fit(_p(conf), _p(al), n, gamma, grid, bins, _p(T), _p(e))
+    return dict(rc=rc, T=T, ece=e)

@@ -377,14 +377,30 @@ static int check_sched_args(const float* conf, int B, int gamma, const double* k
     return OR_OK;
 }
 
+/* [US] §2.4 / §3.6 (STS): the calibrated confidence c^(1/T_k) of position k;
+ * T == NULL leaves the confidence as it is. */
+static double calibrated(float c, const double* T, int k) {
+    return T ? pow((double)c, 1.0 / T[k - 1]) : (double)c;
+}
+
 /* [AS] eq. (20): s_{b,0} = 1, s_{b,k} = prod_{t<=k} c_{b,t}, products taken
  * left to right in fp64.  s has gamma + 1 entries per request. */
+static const double* g_sts_T = NULL; /* calibration temperatures of the call in progress */
+
 static void prefix_survival(const float* conf, int B, int gamma, double* s) {
     for (int b = 0; b < B; ++b) {
         double* sb = s + (int64_t)b * (gamma + 1);
         sb[0] = 1.0;
-        for (int k = 1; k <= gamma; ++k) sb[k] = sb[k - 1] * (double)conf[(int64_t)b * gamma + k - 1];
+        for (int k = 1; k <= gamma; ++k)
+            sb[k] = sb[k - 1] * calibrated(conf[(int64_t)b * gamma + k - 1], g_sts_T, k);
     }
+}
+
+/* Selects the calibration temperatures (or NULL) used by the scheduler
+ * functions below until the next call. */
+int oracle_set_sts(const double* T) {
+    g_sts_T = T;
+    return OR_OK;
 }
 
 /* [AS] eq. (21): estimated progress A_b(n) = sum_{k=0}^{n} s_{b,k}, left to right. */
@@ -562,5 +578,140 @@ int oracle_sched_brute(const float* conf, int B, int gamma, const double* kt, co
     if (out_gap) *out_gap = (best - second) / best;
     free(s);
     free(cur);
+    return OR_OK;
+}
+
+/* D-cut ([AS] §4.2, eqs. (22)-(24)): the budget is restricted to the ratios
+ * rho_i of the full verification budget B(gamma+1): K_i = max(B(min_len+1),
+ * ceil(rho_i * B(gamma+1))); top-K_i selection (the same candidate order as
+ * the exact scan) gives the estimated progress U_i = tau(K_i), summed left to
+ * right in sorted order; the chosen ratio is the first maximum of U_i / C_i.
+ * ratios strictly increasing in (0, 1], costs positive. */
+int oracle_sched_dcut(const float* conf, int B, int gamma, const double* ratios, const double* costs, int nr,
+                      int min_len, int32_t* out_len, int32_t* out_choice) {
+    if (nr < 1 || nr > 32) return OR_ERR_COST_TABLE;
+    for (int i = 0; i < nr; ++i) {
+        if (!(ratios[i] > 0.0 && ratios[i] <= 1.0) || !(costs[i] > 0.0) || !isfinite(costs[i]))
+            return OR_ERR_COST_TABLE;
+        if (i > 0 && !(ratios[i] > ratios[i - 1])) return OR_ERR_COST_TABLE;
+    }
+    int st = check_sched_args(conf, B, gamma, ratios, costs, nr, min_len);
+    if (st != OR_OK) return st;
+    if (B == 0) return OR_OK;
+    double* s;
+    cand_t* c;
+    int64_t nc;
+    double base;
+    st = sched_setup(conf, B, gamma, min_len, &s, &c, &nc, &base);
+    if (st != OR_OK) return st;
+    const double N0 = (double)B * (double)(min_len + 1);
+    const double Nmax = (double)B * (double)(gamma + 1);
+    double best = -INFINITY;
+    int choice = -1;
+    int64_t bestK = 0;
+    for (int i = 0; i < nr; ++i) {
+        double K = ceil(ratios[i] * Nmax);
+        if (K < N0) K = N0;
+        if (K > Nmax) K = Nmax;
+        const int64_t take = (int64_t)(K - N0);
+        double tau = base;
+        for (int64_t k = 0; k < take; ++k) tau += c[k].s;
+        const double obj = tau / costs[i];
+        if (obj > best) {
+            best = obj;
+            choice = i;
+            bestK = take;
+        }
+    }
+    for (int b = 0; b < B; ++b) out_len[b] = min_len;
+    for (int64_t i = 0; i < bestK; ++i) out_len[c[i].b] += 1;
+    if (out_choice) *out_choice = choice;
+    free(s);
+    free(c);
+    return OR_OK;
+}
+
+/* Static threshold scheduler ([BL] "Verify smarter, not longer": a static
+ * confidence threshold, zero recovering fixed-length verification; [US] §3.5
+ * StaticScheduler): each request keeps its leading positions whose confidence
+ * (calibrated if temperatures are set) is at least the threshold, and at
+ * least min_len of them. */
+int oracle_sched_threshold(const float* conf, int B, int gamma, double threshold, int min_len, int32_t* out_len) {
+    if (B < 0 || gamma < 0 || min_len < 0 || min_len > gamma) return OR_ERR_SHAPE;
+    for (int64_t i = 0; i < (int64_t)B * gamma; ++i)
+        if (!(conf[i] >= 0.0f && conf[i] <= 1.0f)) return OR_ERR_CONFIDENCE;
+    for (int b = 0; b < B; ++b) {
+        int n = 0;
+        while (n < gamma && calibrated(conf[(int64_t)b * gamma + n], g_sts_T, n + 1) >= threshold) ++n;
+        out_len[b] = n < min_len ? min_len : n;
+    }
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------- STS
+ * Sequential Temperature Scaling ([US] §2.4 and §3.6): left to right over
+ * positions k = 1..gamma, choose T_k on the grid T = (i+1)/10, i = 0..99 (the
+ * 100 points of linspace(0.1, 10, 100)) minimising the expected calibration
+ * error of the cumulative survival a_k = prod_{j<k} c_j^(1/T_j) * c_k^(1/T)
+ * against the cumulative acceptance labels y_k = [accept_len >= k]; earlier
+ * positions keep their chosen temperatures; ties go to the smaller T.
+ * ECE with `bins` equal-width bins on [0, 1]: sum over bins of
+ * |sum of a - sum of y| / n (equivalently the count-weighted gap of means). */
+static double ece(const double* a, const int* y, int n, int bins, double* sa, double* sy) {
+    for (int k = 0; k < bins; ++k) sa[k] = sy[k] = 0.0;
+    for (int i = 0; i < n; ++i) {
+        int k = (int)(a[i] * (double)bins);
+        if (k >= bins) k = bins - 1;
+        if (k < 0) k = 0;
+        sa[k] += a[i];
+        sy[k] += (double)y[i];
+    }
+    double e = 0.0;
+    for (int k = 0; k < bins; ++k) e += fabs(sa[k] - sy[k]);
+    return e / (double)n;
+}
+
+int oracle_sts_ece(const double* a, const int32_t* y, int n, int bins, double* out) {
+    double* sa = (double*)malloc(sizeof(double) * (size_t)bins);
+    double* sy = (double*)malloc(sizeof(double) * (size_t)bins);
+    int* yy = (int*)malloc(sizeof(int) * (size_t)n);
+    for (int i = 0; i < n; ++i) yy[i] = y[i];
+    *out = ece(a, yy, n, bins, sa, sy);
+    free(sa);
+    free(sy);
+    free(yy);
+    return OR_OK;
+}
+
+int oracle_sts_fit(const float* conf, const int32_t* accept_len, int n, int gamma, int grid, int bins,
+                   double* out_T, double* out_ece) {
+    if (n < 1 || gamma < 1 || gamma > 63 || grid < 1 || bins < 1) return OR_ERR_SHAPE;
+    double* prefix = (double*)malloc(sizeof(double) * (size_t)n); /* prod_{j<k} c_j^(1/T_j) */
+    double* a = (double*)malloc(sizeof(double) * (size_t)n);
+    int* y = (int*)malloc(sizeof(int) * (size_t)n);
+    double* sa = (double*)malloc(sizeof(double) * (size_t)bins);
+    double* sy = (double*)malloc(sizeof(double) * (size_t)bins);
+    for (int i = 0; i < n; ++i) prefix[i] = 1.0;
+    for (int k = 1; k <= gamma; ++k) {
+        for (int i = 0; i < n; ++i) y[i] = accept_len[i] >= k ? 1 : 0;
+        double best = INFINITY, bestT = 1.0;
+        for (int g = 0; g < grid; ++g) {
+            const double T = (double)(g + 1) / 10.0;
+            for (int i = 0; i < n; ++i) a[i] = prefix[i] * pow((double)conf[(int64_t)i * gamma + k - 1], 1.0 / T);
+            const double e = ece(a, y, n, bins, sa, sy);
+            if (e < best) {
+                best = e;
+                bestT = T;
+            }
+        }
+        out_T[k - 1] = bestT;
+        if (out_ece) out_ece[k - 1] = best;
+        for (int i = 0; i < n; ++i) prefix[i] *= pow((double)conf[(int64_t)i * gamma + k - 1], 1.0 / bestT);
+    }
+    free(prefix);
+    free(a);
+    free(y);
+    free(sa);
+    free(sy);
     return OR_OK;
 }

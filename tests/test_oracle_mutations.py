@@ -36,13 +36,21 @@ MUTATIONS = {
                                "if (!have || z >= m) { m = z; a = v; have = 1; }"),
     "sched_ties_deep_first": ("if (a->k != c->k) return a->k < c->k ? -1 : 1;",
                               "if (a->k != c->k) return a->k > c->k ? -1 : 1;"),
-    "survival_index_shifted": ("sb[k] = sb[k - 1] * (double)conf[(int64_t)b * gamma + k - 1];",
-                               "sb[k] = sb[k - 1] * (double)conf[(int64_t)b * gamma + (k > 1 ? k - 2 : 0)];"),
+    "survival_index_shifted": ("sb[k - 1] * calibrated(conf[(int64_t)b * gamma + k - 1], g_sts_T, k);",
+                               "sb[k - 1] * calibrated(conf[(int64_t)b * gamma + (k > 1 ? k - 2 : 0)], g_sts_T, k);"),
     "cost_slope_sign": ("return kc[i] + ((N - kt[i]) * (kc[i + 1] - kc[i])) / (kt[i + 1] - kt[i]);",
                         "return kc[i] + ((N - kt[i]) * (kc[i + 1] + kc[i])) / (kt[i + 1] - kt[i]);"),
     "exact_last_max": ("if (obj > best) { best = obj; bestK = i + 1; }",
                        "if (obj >= best) { best = obj; bestK = i + 1; }"),
     "alg1_no_revert": ("out_len[r] = c[i].k - 1; /* early stop", "/* early stop"),
+    "dcut_floor_budget": ("double K = ceil(ratios[i] * Nmax);", "double K = floor(ratios[i] * Nmax);"),
+    "dcut_last_max": ("        if (obj > best) {\n            best = obj;\n            choice = i;",
+                      "        if (obj >= best) {\n            best = obj;\n            choice = i;"),
+    "threshold_strict": ("g_sts_T, n + 1) >= threshold) ++n;", "g_sts_T, n + 1) > threshold) ++n;"),
+    "ece_no_abs": ("for (int k = 0; k < bins; ++k) e += fabs(sa[k] - sy[k]);",
+                   "for (int k = 0; k < bins; ++k) e += sa[k] - sy[k];"),
+    "sts_power_inverted": ("a[i] = prefix[i] * pow((double)conf[(int64_t)i * gamma + k - 1], 1.0 / T);",
+                           "a[i] = prefix[i] * pow((double)conf[(int64_t)i * gamma + k - 1], T);"),
 }
 
 
@@ -60,6 +68,7 @@ def test_pins_catch_planted_mistake(name, tmp_path):
     env = dict(os.environ, SPECV_ORACLE_LIB=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_verify.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_sched.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_sched.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_sched_ext.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"pins did not catch mutation {name}:\n{r.stdout[-2000:]}"
