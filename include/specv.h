@@ -149,7 +149,12 @@ typedef struct {
 
 typedef enum {
     SPEC_SCHED_EXACT = 0,      /* first budget N that maximises tau(N)/C(N) over every N */
-    SPEC_SCHED_ALGORITHM1 = 1  /* Algorithm 1: add candidates while tau/C strictly improves */
+    SPEC_SCHED_ALGORITHM1 = 1, /* Algorithm 1: add candidates while tau/C strictly improves */
+    SPEC_SCHED_DCUT = 2        /* D-cut: the table's "tokens" are budget ratios rho_i in (0, 1]
+                                  (strictly increasing) and its costs C(B, rho_i); the budget is
+                                  K_i = max(B(min_len+1), ceil(rho_i * B(gamma+1))) and the first
+                                  maximum of tau(K_i) / C_i is taken ("AngelSpec" §4.2,
+                                  eqs. (22)-(24)) */
 } spec_sched_mode;
 
 /* Bytes of device workspace spec_schedule needs (its status word). */
@@ -160,14 +165,47 @@ size_t spec_schedule_workspace_bytes(int B, int gamma);
  *   confidence      [B, gamma] fp32 in [0, 1]; confidence[b][k-1] is c_{b,k}.
  *   cost            HOST pointer, copied by value into the launch.
  *   min_len         every request keeps at least min_len drafts (0 <= min_len <= gamma).
+ *   sts_temperature HOST [gamma] fp32 > 0 or NULL: Sequential Temperature
+ *                   Scaling ("UraionSpec" §2.4): the scheduler uses the calibrated
+ *                   confidence c_{b,k}^(1/T_k) (fp64 pow) in place of c_{b,k}.
  *   out_verify_len  [B] int32 in [min_len, gamma] (all -1 if a confidence is invalid).
  * Arithmetic is fp64 with a fixed order (left-to-right products and sums, the
  * budget prefix summed in sorted order), so results are reproducible bit for
  * bit.  Requires B <= 4096, gamma <= 32, B * (gamma - min_len) <= 16384.
  */
 int spec_schedule(const float* confidence, int B, int gamma, const spec_cost_table* cost,
-                  int min_len, spec_sched_mode mode, int32_t* out_verify_len, void* workspace,
-                  size_t workspace_bytes, spec_stream_t stream);
+                  int min_len, spec_sched_mode mode, const float* sts_temperature,
+                  int32_t* out_verify_len, void* workspace, size_t workspace_bytes,
+                  spec_stream_t stream);
+
+/*
+ * Static verify lengths ("breaking down dspark and its lineage", section
+ * "Verify smarter, not longer": a static confidence threshold, zero recovering
+ * fixed-length verification; "UraionSpec" §3.5, the fixed-length and
+ * static-threshold StaticScheduler).  Request b keeps its leading positions k
+ * whose (optionally STS-calibrated) confidence is at least `threshold`, at most
+ * max_len and at least min_len of them: threshold <= 0 gives fixed length
+ * max_len, and then confidence may be NULL.  0 <= min_len <= max_len <= gamma.
+ * Requests are independent: one with a confidence outside [0, 1] (or NaN) gets
+ * verify length -1 and the status word SPEC_ERR_CONFIDENCE; the others are
+ * scheduled as usual.  Other arguments as for spec_schedule; any B <= 4096.
+ */
+int spec_schedule_static(const float* confidence, int B, int gamma, float threshold, int max_len,
+                         int min_len, const float* sts_temperature, int32_t* out_verify_len,
+                         void* workspace, size_t workspace_bytes, spec_stream_t stream);
+
+/*
+ * Host-side STS fit ("UraionSpec" §2.4 and §3.6): for positions k = 1..gamma
+ * in order, the temperature T_k on the grid (i+1)/10, i = 0..99 (the 100
+ * points of 0.1..10) minimising the 15-bin expected calibration error of the
+ * cumulative survival prod_{j<k} c_j^(1/T_j) * c_k^(1/T) against the labels
+ * [accept_len >= k]; earlier positions keep their chosen T; ties go to the
+ * smaller T.  All HOST pointers: confidence [n, gamma] fp32, accept_len [n]
+ * int32 (observed with verify_len = gamma), out_temperature [gamma] fp32,
+ * out_ece [gamma] fp64 or NULL.  Runs on the CPU, fp64.
+ */
+int spec_sts_fit(const float* confidence, const int32_t* accept_len, int n, int gamma,
+                 float* out_temperature, double* out_ece);
 
 /* ------------------------------------------------- verification, no workspace */
 

@@ -54,8 +54,8 @@ def _L():
         lib.oracle_sched_alg1.argtypes = [vp, i32, i32, vp, vp, i32, i32, vp]
         lib.oracle_sched_brute.argtypes = [vp, i32, i32, vp, vp, i32, i32, vp, vp, vp]
         lib.oracle_set_sts.argtypes = [vp]
-        lib.oracle_sched_dcut.argtypes = [vp, i32, i32, vp, vp, i32, i32, vp, vp]
-        lib.oracle_sched_threshold.argtypes = [vp, i32, i32, dbl, i32, vp]
+        lib.oracle_sched_dcut.argtypes = [vp, i32, i32, vp, vp, i32, i32, vp, vp, vp]
+        lib.oracle_sched_threshold.argtypes = [vp, i32, i32, dbl, i32, i32, vp]
         lib.oracle_sts_ece.argtypes = [vp, vp, i32, i32, vp]
         lib.oracle_sts_fit.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp]
         for f in ("oracle_verify", "oracle_verify_probs", "oracle_cost_at", "oracle_sched_exact",
@@ -179,16 +179,19 @@ def sched_dcut(conf, ratios, costs, min_len: int = 0, sts_T=None) -> dict:
     c = np.ascontiguousarray(costs, np.float64)
     out = np.full(B, -1, np.int32)
     choice = ctypes.c_int(-1)
-    rc = _L().oracle_sched_dcut(_p(conf), B, gamma, _p(r), _p(c), len(r), min_len, _p(out), ctypes.byref(choice))
-    return dict(rc=rc, verify_len=out, choice=choice.value)
+    obj = np.full(len(r), np.nan)
+    rc = _L().oracle_sched_dcut(_p(conf), B, gamma, _p(r), _p(c), len(r), min_len, _p(out), ctypes.byref(choice),
+                                _p(obj))
+    return dict(rc=rc, verify_len=out, choice=choice.value, obj=obj)
 
 
-def sched_threshold(conf, threshold: float, min_len: int = 0, sts_T=None) -> dict:
+def sched_threshold(conf, threshold: float, min_len: int = 0, sts_T=None, max_len: int | None = None) -> dict:
     _set_sts(sts_T)
     conf = np.ascontiguousarray(conf, np.float32)
     B, gamma = conf.shape
     out = np.full(B, -1, np.int32)
-    rc = _L().oracle_sched_threshold(_p(conf), B, gamma, float(threshold), min_len, _p(out))
+    ml = gamma if max_len is None else max_len
+    rc = _L().oracle_sched_threshold(_p(conf), B, gamma, float(threshold), ml, min_len, _p(out))
     return dict(rc=rc, verify_len=out)
 
 

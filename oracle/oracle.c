@@ -588,7 +588,7 @@ int oracle_sched_brute(const float* conf, int B, int gamma, const double* kt, co
  * right in sorted order; the chosen ratio is the first maximum of U_i / C_i.
  * ratios strictly increasing in (0, 1], costs positive. */
 int oracle_sched_dcut(const float* conf, int B, int gamma, const double* ratios, const double* costs, int nr,
-                      int min_len, int32_t* out_len, int32_t* out_choice) {
+                      int min_len, int32_t* out_len, int32_t* out_choice, double* out_obj) {
     if (nr < 1 || nr > 32) return OR_ERR_COST_TABLE;
     for (int i = 0; i < nr; ++i) {
         if (!(ratios[i] > 0.0 && ratios[i] <= 1.0) || !(costs[i] > 0.0) || !isfinite(costs[i]))
@@ -617,6 +617,7 @@ int oracle_sched_dcut(const float* conf, int B, int gamma, const double* ratios,
         double tau = base;
         for (int64_t k = 0; k < take; ++k) tau += c[k].s;
         const double obj = tau / costs[i];
+        if (out_obj) out_obj[i] = obj;
         if (obj > best) {
             best = obj;
             choice = i;
@@ -633,16 +634,19 @@ int oracle_sched_dcut(const float* conf, int B, int gamma, const double* ratios,
 
 /* Static threshold scheduler ([BL] "Verify smarter, not longer": a static
  * confidence threshold, zero recovering fixed-length verification; [US] §3.5
- * StaticScheduler): each request keeps its leading positions whose confidence
- * (calibrated if temperatures are set) is at least the threshold, and at
- * least min_len of them. */
-int oracle_sched_threshold(const float* conf, int B, int gamma, double threshold, int min_len, int32_t* out_len) {
-    if (B < 0 || gamma < 0 || min_len < 0 || min_len > gamma) return OR_ERR_SHAPE;
+ * StaticScheduler with fixed-length and static-threshold modes): each request
+ * keeps its leading positions whose confidence (calibrated if temperatures are
+ * set) is at least the threshold, at most max_len and at least min_len of them;
+ * threshold 0 with max_len L is fixed-length verification of L drafts. */
+int oracle_sched_threshold(const float* conf, int B, int gamma, double threshold, int max_len, int min_len,
+                           int32_t* out_len) {
+    if (B < 0 || gamma < 0 || min_len < 0 || min_len > gamma || max_len < min_len || max_len > gamma)
+        return OR_ERR_SHAPE;
     for (int64_t i = 0; i < (int64_t)B * gamma; ++i)
         if (!(conf[i] >= 0.0f && conf[i] <= 1.0f)) return OR_ERR_CONFIDENCE;
     for (int b = 0; b < B; ++b) {
         int n = 0;
-        while (n < gamma && calibrated(conf[(int64_t)b * gamma + n], g_sts_T, n + 1) >= threshold) ++n;
+        while (n < max_len && calibrated(conf[(int64_t)b * gamma + n], g_sts_T, n + 1) >= threshold) ++n;
         out_len[b] = n < min_len ? min_len : n;
     }
     return OR_OK;

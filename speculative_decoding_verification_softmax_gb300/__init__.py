@@ -27,13 +27,13 @@ OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_TEMPERATURE = 0, -1, -2, -3, -4
 ERR_VERIFY_LEN, ERR_TOKEN, ERR_WORKSPACE, ERR_COST_TABLE = -5, -6, -7, -8
 ERR_NONFINITE, ERR_TIMEOUT, ERR_CUDA, ERR_UNIFORM, ERR_CONFIDENCE = -9, -10, -11, -12, -13
 F32, BF16 = 0, 1
-SCHED_EXACT, SCHED_ALGORITHM1 = 0, 1
+SCHED_EXACT, SCHED_ALGORITHM1, SCHED_DCUT = 0, 1, 2
 MAX_BATCH, MAX_GAMMA, MAX_SCHED_CANDIDATES = 4096, 32, 16384
 
 EXPORTED = ["spec_verify_workspace_bytes", "spec_verify", "spec_verify_stats",
             "spec_schedule_workspace_bytes", "spec_schedule", "spec_read_status",
             "spec_status_string", "spec_profile_events", "spec_verify_kernel_count",
-            "spec_verify_static"]
+            "spec_verify_static", "spec_schedule_static", "spec_sts_fit"]
 STATIC_WORKSPACE_BYTES = 8 << 20
 
 
@@ -104,7 +104,11 @@ def lib():
                 L.spec_verify_stats.restype = i32
                 L.spec_schedule_workspace_bytes.argtypes = [i32, i32]
                 L.spec_schedule_workspace_bytes.restype = sz
-                L.spec_schedule.argtypes = [vp, i32, i32, vp, i32, i32, vp, vp, sz, vp]
+                L.spec_schedule.argtypes = [vp, i32, i32, vp, i32, i32, vp, vp, vp, sz, vp]
+                L.spec_schedule_static.argtypes = [vp, i32, i32, f32, i32, i32, vp, vp, vp, sz, vp]
+                L.spec_schedule_static.restype = i32
+                L.spec_sts_fit.argtypes = [vp, vp, i32, i32, vp, vp]
+                L.spec_sts_fit.restype = i32
                 L.spec_schedule.restype = i32
                 L.spec_read_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
                 L.spec_read_status.restype = i32
@@ -261,10 +265,21 @@ def verify_stats(workspace, B: int, gamma: int, V: int, dtype_code: int, stream=
     return px, qx, mass, st
 
 
-def schedule(confidence, cost, min_len: int = 0, mode: int = SCHED_EXACT, *, out_verify_len=None,
+def _sts_arg(sts, gamma):
+    if sts is None:
+        return None, None
+    import numpy as np
+    arr = np.ascontiguousarray(np.asarray(sts, dtype=np.float32).reshape(-1))
+    if arr.size != gamma:
+        raise ValueError("sts temperatures need one value per draft position")
+    return arr, arr.ctypes.data_as(ctypes.c_void_p)
+
+
+def schedule(confidence, cost, min_len: int = 0, mode: int = SCHED_EXACT, *, sts=None, out_verify_len=None,
              workspace=None, stream=None):
     """Run spec_schedule: confidence [B, gamma] fp32 CUDA tensor, cost = (tokens, cost_ms)
-    knots or a CostTable.  Returns (out_verify_len [B] int32, workspace)."""
+    knots or a CostTable (for SCHED_DCUT: (ratios, costs)); sts = per-position STS
+    temperatures or None.  Returns (out_verify_len [B] int32, workspace)."""
     torch = _torch()
     B, gamma = confidence.shape
     if not confidence.is_cuda or not confidence.is_contiguous() or confidence.dtype != torch.float32:
@@ -275,11 +290,45 @@ def schedule(confidence, cost, min_len: int = 0, mode: int = SCHED_EXACT, *, out
     if workspace is None:
         workspace = torch.zeros(max(256, int(lib().spec_schedule_workspace_bytes(B, gamma))),
                                 dtype=torch.uint8, device=confidence.device)
-    rc = lib().spec_schedule(_ptr(confidence), B, gamma, ctypes.byref(table), min_len, mode,
+    keep, sts_p = _sts_arg(sts, gamma)
+    rc = lib().spec_schedule(_ptr(confidence), B, gamma, ctypes.byref(table), min_len, mode, sts_p,
                              _ptr(out_verify_len), _ptr(workspace), workspace.numel(),
                              _stream_handle(stream))
     _check(rc, "spec_schedule")
     return out_verify_len, workspace
+
+
+def schedule_static(confidence, threshold: float, max_len: int, min_len: int = 0, *, sts=None,
+                    out_verify_len=None, workspace=None, stream=None):
+    """Run spec_schedule_static: leading positions with confidence >= threshold,
+    clamped to [min_len, max_len] (threshold <= 0: fixed length max_len)."""
+    torch = _torch()
+    B, gamma = confidence.shape
+    if out_verify_len is None:
+        out_verify_len = torch.empty((B,), dtype=torch.int32, device=confidence.device)
+    if workspace is None:
+        workspace = torch.zeros(256, dtype=torch.uint8, device=confidence.device)
+    keep, sts_p = _sts_arg(sts, gamma)
+    rc = lib().spec_schedule_static(_ptr(confidence), B, gamma, ctypes.c_float(threshold), max_len, min_len, sts_p,
+                                    _ptr(out_verify_len), _ptr(workspace), workspace.numel(),
+                                    _stream_handle(stream))
+    _check(rc, "spec_schedule_static")
+    return out_verify_len, workspace
+
+
+def sts_fit(confidence, accept_len):
+    """spec_sts_fit on host arrays: confidences [n, gamma] and the accept lengths
+    observed at verify_len = gamma.  Returns (temperatures [gamma] fp32, ece [gamma])."""
+    import numpy as np
+    c = np.ascontiguousarray(confidence, np.float32)
+    al = np.ascontiguousarray(accept_len, np.int32)
+    n, gamma = c.shape
+    T = np.empty(gamma, np.float32)
+    e = np.empty(gamma, np.float64)
+    rc = lib().spec_sts_fit(c.ctypes.data_as(ctypes.c_void_p), al.ctypes.data_as(ctypes.c_void_p), n, gamma,
+                            T.ctypes.data_as(ctypes.c_void_p), e.ctypes.data_as(ctypes.c_void_p))
+    _check(rc, "spec_sts_fit")
+    return T, e
 
 
 def read_status(workspace, stream=None) -> int:

@@ -1,5 +1,8 @@
 // Status word access and status strings of the C ABI.
 #include <cuda_runtime.h>
+#include <math.h>
+
+#include <vector>
 
 #include "specv_common.cuh"
 
@@ -15,6 +18,44 @@ int spec_read_status(void* workspace, spec_stream_t stream, int* status) {
     if (cudaStreamSynchronize(st) != cudaSuccess) return SPEC_ERR_CUDA;
     if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return SPEC_ERR_CUDA;
     *status = v;
+    return SPEC_OK;
+}
+
+// Sequential Temperature Scaling fit on the host ("UraionSpec" §2.4, §3.6).
+int spec_sts_fit(const float* confidence, const int32_t* accept_len, int n, int gamma, float* out_temperature,
+                 double* out_ece) {
+    if (n < 1 || gamma < 1 || gamma > SPEC_MAX_GAMMA) return SPEC_ERR_SHAPE;
+    if (!confidence || !accept_len || !out_temperature) return SPEC_ERR_NULL;
+    for (long long i = 0; i < (long long)n * gamma; ++i)
+        if (!(confidence[i] >= 0.0f && confidence[i] <= 1.0f)) return SPEC_ERR_CONFIDENCE;
+    constexpr int kGrid = 100, kBins = 15;
+    std::vector<double> survived(n, 1.0);  // prod over calibrated earlier positions
+    std::vector<double> pred(n);
+    double in_bin_pred[kBins], in_bin_label[kBins];
+    for (int k = 1; k <= gamma; ++k) {
+        double best_err = INFINITY, best_t = 1.0;
+        for (int g = 0; g < kGrid; ++g) {
+            const double t = (double)(g + 1) / 10.0;  // 0.1, 0.2, ..., 10.0
+            for (int i = 0; i < n; ++i) pred[i] = survived[i] * pow((double)confidence[(size_t)i * gamma + k - 1], 1.0 / t);
+            for (int q = 0; q < kBins; ++q) in_bin_pred[q] = in_bin_label[q] = 0.0;
+            for (int i = 0; i < n; ++i) {
+                int q = (int)(pred[i] * (double)kBins);
+                q = q < 0 ? 0 : (q >= kBins ? kBins - 1 : q);
+                in_bin_pred[q] += pred[i];
+                in_bin_label[q] += accept_len[i] >= k ? 1.0 : 0.0;
+            }
+            double err = 0.0;
+            for (int q = 0; q < kBins; ++q) err += fabs(in_bin_pred[q] - in_bin_label[q]);
+            err /= (double)n;
+            if (err < best_err) {
+                best_err = err;
+                best_t = t;
+            }
+        }
+        out_temperature[k - 1] = (float)best_t;
+        if (out_ece) out_ece[k - 1] = best_err;
+        for (int i = 0; i < n; ++i) survived[i] *= pow((double)confidence[(size_t)i * gamma + k - 1], 1.0 / best_t);
+    }
     return SPEC_OK;
 }
 

@@ -88,12 +88,13 @@ def test_schedule_host_errors(L):
 
     def sched(B=4, gamma=4, cost=table, min_len=0, mode=0, conf=FAKE, out=FAKE, ws=FAKE, ws_bytes=256):
         return L.spec_schedule(conf, B, gamma, ctypes.byref(cost) if cost is not None else None,
-                               min_len, mode, out, ws, ws_bytes, None)
+                               min_len, mode, None, out, ws, ws_bytes, None)
 
     assert sched(B=-1) == sv.ERR_SHAPE
     assert sched(min_len=5) == sv.ERR_SHAPE
     assert sched(B=4096, gamma=32) == sv.ERR_SHAPE         # more than 16384 candidates
-    assert sched(mode=2) == sv.ERR_SHAPE
+    assert sched(mode=3) == sv.ERR_SHAPE
+    assert sched(mode=2) == sv.ERR_COST_TABLE                # knots 512 and 513 are not ratios in (0, 1]
     assert sched(cost=None) == sv.ERR_NULL
     assert sched(cost=sv.CostTable.from_knots([1.0, 1.0], [1.0, 2.0])) == sv.ERR_COST_TABLE
     assert sched(cost=sv.CostTable.from_knots([0.0, 1.0], [1.0, 0.0])) == sv.ERR_COST_TABLE
@@ -101,6 +102,32 @@ def test_schedule_host_errors(L):
     assert sched(ws_bytes=8) == sv.ERR_WORKSPACE
     assert sched(ws=ctypes.c_void_p(0x10004)) == sv.ERR_ALIGN
     assert sched(B=0, conf=None, out=None, ws=None) == sv.OK
+
+
+def test_schedule_static_host_errors(L):
+    T = (ctypes.c_float * 4)(1.0, 0.5, 2.0, 1.0)
+    Tbad = (ctypes.c_float * 4)(1.0, 0.0, 2.0, 1.0)
+
+    def st(B=4, gamma=4, th=0.5, max_len=4, min_len=0, sts=None, conf=FAKE, out=FAKE, ws=FAKE, ws_bytes=256):
+        return L.spec_schedule_static(conf, B, gamma, ctypes.c_float(th), max_len, min_len, sts, out, ws,
+                                      ws_bytes, None)
+
+    assert st(B=-1) == sv.ERR_SHAPE
+    assert st(max_len=5) == sv.ERR_SHAPE
+    assert st(min_len=3, max_len=2) == sv.ERR_SHAPE
+    assert st(th=float("nan")) == sv.ERR_SHAPE
+    assert st(sts=Tbad) == sv.ERR_SHAPE
+    assert st(conf=None) == sv.ERR_NULL
+    assert st(ws=ctypes.c_void_p(0x10004)) == sv.ERR_ALIGN
+    assert st(sts=T, ws_bytes=8) == sv.ERR_WORKSPACE
+    assert st(B=0, conf=None, out=None, ws=None) == sv.OK
+
+
+def test_schedule_rejects_bad_temperatures(L):
+    table = sv.CostTable.from_knots([0.0, 512.0], [8.0, 18.24])
+    for bad in (0.0, -1.0, float("inf"), float("nan")):
+        T = (ctypes.c_float * 4)(1.0, 1.0, bad, 1.0)
+        assert L.spec_schedule(FAKE, 4, 4, ctypes.byref(table), 0, 0, T, FAKE, FAKE, 256, None) == sv.ERR_SHAPE
 
 
 def test_status_strings(L):

@@ -105,6 +105,12 @@ def test_threshold_keeps_the_leading_run():
     assert list(oracle.sched_threshold(np.array([[0.5, 0.5, 0.25]], np.float32), 0.5)["verify_len"]) == [2]
 
 
+def test_fixed_length_mode():
+    conf = specsynth.make_confidences(16, 8, seed=1)
+    assert (oracle.sched_threshold(conf, 0.0, max_len=3)["verify_len"] == 3).all()
+    assert (oracle.sched_threshold(conf, 0.0, min_len=2, max_len=2)["verify_len"] == 2).all()
+
+
 def test_threshold_is_monotone():
     conf = specsynth.make_confidences(64, 16, seed=2)
     prev = None
