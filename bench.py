@@ -206,6 +206,68 @@ def workload_config(case):
             "l2": f"inputs larger than L2 ({logit_bytes / 1e6:.1f} MB of logits read per step)"}
 
 
+SCHED_REPLAYS = 200
+
+
+def time_schedulers(sv, dev, stream, rank: int):
+    """Device time per call of each scheduler on the scheduled workload
+    (B=64, gamma=16 confidences, min_len=1): SCHED_REPLAYS calls captured in one
+    CUDA graph, replayed, timed with CUDA events on the launching stream."""
+    import torch
+    import specsynth
+    conf = specsynth.make_confidences(seed=specsynth.SCHED_SEED + 1000 * rank)
+    B, gamma = conf.shape
+    c = torch.from_numpy(conf).to(dev)
+    out = torch.empty((B,), dtype=torch.int32, device=dev)
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    cost = specsynth.COST_TABLES["Bprime"]
+    ratios, rcost = [0.25, 0.5, 0.75, 1.0], [10.0, 13.0, 16.0, 19.0]
+    sts = np.linspace(0.8, 1.6, gamma).astype(np.float32)
+    ml = specsynth.SCHED_MIN_LEN
+    modes = {
+        "exact": lambda: sv.schedule(c, cost, ml, sv.SCHED_EXACT, out_verify_len=out, workspace=ws),
+        "algorithm1": lambda: sv.schedule(c, cost, ml, sv.SCHED_ALGORITHM1, out_verify_len=out, workspace=ws),
+        "dcut": lambda: sv.schedule(c, (ratios, rcost), ml, sv.SCHED_DCUT, out_verify_len=out, workspace=ws),
+        "exact_sts": lambda: sv.schedule(c, cost, ml, sv.SCHED_EXACT, sts=sts, out_verify_len=out, workspace=ws),
+        "static_threshold": lambda: sv.schedule_static(c, 0.6, gamma, ml, out_verify_len=out, workspace=ws),
+        "static_threshold_sts": lambda: sv.schedule_static(c, 0.6, gamma, ml, sts=sts, out_verify_len=out,
+                                                           workspace=ws),
+    }
+    res = {}
+    for name, call in modes.items():
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize(dev)
+        if sv.read_status(ws) != 0:
+            raise RuntimeError(f"scheduler status ({name})")
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                for _ in range(SCHED_REPLAYS):
+                    call()
+        stream.wait_stream(side)
+        g.replay()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(side):
+            e0.record(side)
+            for _ in range(5):
+                g.replay()
+            e1.record(side)
+        torch.cuda.synchronize(dev)
+        res[name] = {"us_per_call": e0.elapsed_time(e1) * 1e3 / (5 * SCHED_REPLAYS),
+                     "mean_verify_len": float(out.float().mean().item())}
+        if sv.read_status(ws) != 0:
+            raise RuntimeError(f"scheduler status after replay ({name})")
+    return {"workload": f"scheduled ragged: B={B}, gamma={gamma} confidences sigmoid(N(1.5, 1)), "
+                        f"min_len={ml}; cost table 8 ms + 0.02 ms/token to 512 tokens, 20 ms above; "
+                        f"D-cut ratios {ratios} with costs {rcost} ms; STS temperatures 0.8..1.6",
+            "timing": f"{SCHED_REPLAYS} calls per CUDA graph, 5 replays, CUDA events",
+            "kernel_launches_per_call": 1, "modes": res}
+
+
 def run_ours(args):
     import torch
     import specsynth
@@ -275,6 +337,38 @@ def run_ours(args):
     status = sv.read_status(ws)
     n = out_n.cpu().numpy()
 
+    # the whole path on the scheduled ragged workload: spec_schedule (exact
+    # scan, cost table B', min_len 1) feeding spec_verify, back to back
+    conf_s = torch.from_numpy(specsynth.make_confidences(seed=specsynth.SCHED_SEED + 1000 * rank)).to(dev)
+    vl_s = torch.empty((B,), dtype=torch.int32, device=dev)
+    ws_s = torch.zeros(256, dtype=torch.uint8, device=dev)
+    cost_s = specsynth.COST_TABLES["Bprime"]
+
+    def sched_step():
+        sv.schedule(conf_s, cost_s, specsynth.SCHED_MIN_LEN, sv.SCHED_EXACT, out_verify_len=vl_s, workspace=ws_s)
+        sv.verify(t, d, x, vl_s, case.T, u, out_tokens=out_t, out_accept_len=out_n, workspace=ws)
+
+    for _ in range(3):
+        sched_step()
+    torch.cuda.synchronize(dev)
+    s_steps = max(3, min(args.steps, 500))
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(s_steps):
+        sched_step()
+    s1.record(stream)
+    torch.cuda.synchronize(dev)
+    s_ms = s0.elapsed_time(s1) / s_steps
+    s_rows = int(vl_s.sum().item())
+    if sv.read_status(ws) != 0 or sv.read_status(ws_s) != 0:
+        raise RuntimeError("device status on the scheduled workload")
+    scheduled_step = {"workload": "schedule (exact scan, cost table B', min_len 1) then verify of the "
+                                  f"{WORKLOAD} logits at the scheduled lengths",
+                      "ms_per_step": s_ms, "verified_rows_per_step": s_rows,
+                      "verified_rows_per_s": s_rows / (s_ms / 1e3), "steps": s_steps,
+                      "kernel_launches_per_step": 1 + sv.kernel_count(B, case.T)}
+    sched = time_schedulers(sv, dev, stream, rank)
+
     # end to end through the public API: pinned host inputs -> device -> verify -> host outputs
     h_t = torch.from_numpy(case.target.view(np.int16)).pin_memory()
     h_d = torch.from_numpy(case.draft.view(np.int16)).pin_memory()
@@ -317,7 +411,7 @@ def run_ours(args):
     rows_per_step = B * gamma
     value = aggregate(ms_max, rows_per_step, world)
     alg_bytes = B * (2 * gamma + 1) * V * 2                      # row-stats kernel, all rows needed
-    rejected = int((n < gamma).sum())
+    rejected = int((n < gamma).sum())      # of the last verify-all call
     resid_bytes = (2 * rejected + (B - rejected)) * V * 2
     peak, peak_kind = measured_peak_gbs()
     achieved = alg_bytes / (k1_ms / 1e3) / 1e9
@@ -342,6 +436,8 @@ def run_ours(args):
         "gpu_launches": sv.kernel_count(B, case.T) * args.steps,
         "clocks": clk.summary(),
         "device_status": status,
+        "scheduled_step": scheduled_step,
+        "schedule": sched,
         "mean_accept_len": float(n.mean()),
     }
     print(json.dumps(line), flush=True)

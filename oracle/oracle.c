@@ -46,6 +46,8 @@
  *     Invalid requests emit accept_len -1 and tokens -1.
  *   - Scheduler budget N = sum_b (ell_b + 1) (bonus positions count) and the
  *     objective is tau(N) / C(N), C a piecewise-linear cost table.
+ *   - Progress sums are exact in fixed point: survivals rounded to multiples
+ *     of 2^-46, summed as 64-bit integers (order-free).
  */
 #include <math.h>
 #include <stdint.h>
@@ -403,22 +405,42 @@ int oracle_set_sts(const double* T) {
     return OR_OK;
 }
 
-/* [AS] eq. (21): estimated progress A_b(n) = sum_{k=0}^{n} s_{b,k}, left to right. */
-static double progress(const double* sb, int n) {
-    double a = 0.0;
-    for (int k = 0; k <= n; ++k) a += sb[k];
+/* Progress in fixed point.  [AS] eq. (21) defines the estimated progress as
+ * the plain sum A_b(n) = sum_{k=0}^{n} s_{b,k}; the pages fix neither its
+ * precision nor its order.  Reading: every survival is rounded (to nearest,
+ * ties to even) to a multiple of 2^-46 and the sums are exact in 64-bit
+ * integers, so a progress value depends only on the set of survivals summed,
+ * never on the order.  Survivals lie in [0, 1] and at most B(gamma+1) <=
+ * 4096 * 33 of them are summed, which stays below 2^64.  A progress enters an
+ * objective as the double nearest to (integer) * 2^-46. */
+#define PROG_FRAC_BITS 46
+typedef uint64_t prog_t;
+
+static prog_t prog_quant(double s) {
+    return (prog_t)rint(ldexp(s, PROG_FRAC_BITS));
+}
+
+static double prog_value(prog_t t) {
+    return ldexp((double)t, -PROG_FRAC_BITS);
+}
+
+static prog_t progress(const double* sb, int n) {
+    prog_t a = 0;
+    for (int k = 0; k <= n; ++k) a += prog_quant(sb[k]);
     return a;
 }
 
-typedef struct { double s; int k; int b; } cand_t;
+typedef struct { prog_t q; int k; int b; } cand_t;
 
 /* Candidate order: survival descending, then shallower position, then lower
- * request index ([AS] §4.2, top-K with ties broken toward shallower positions). */
+ * request index ([AS] §4.2, top-K with ties broken toward shallower positions).
+ * The survival compared is the fixed-point one, the value the progress sums
+ * use. */
 static int cand_cmp(const void* pa, const void* pb) {
     const cand_t* a = (const cand_t*)pa;
     const cand_t* c = (const cand_t*)pb;
-    if (a->s > c->s) return -1;
-    if (a->s < c->s) return 1;
+    if (a->q > c->q) return -1;
+    if (a->q < c->q) return 1;
     if (a->k != c->k) return a->k < c->k ? -1 : 1;
     if (a->b != c->b) return a->b < c->b ? -1 : 1;
     return 0;
@@ -427,18 +449,18 @@ static int cand_cmp(const void* pa, const void* pb) {
 /* Shared set-up of the exact and Algorithm-1 schedulers: survival products,
  * the base progress at min_len, and the sorted candidate list. */
 static int sched_setup(const float* conf, int B, int gamma, int min_len, double** s_out,
-                       cand_t** c_out, int64_t* nc_out, double* base_out) {
+                       cand_t** c_out, int64_t* nc_out, prog_t* base_out) {
     double* s = (double*)malloc(sizeof(double) * (size_t)B * (size_t)(gamma + 1) + 8);
     int64_t nc = (int64_t)B * (gamma - min_len);
     cand_t* c = (cand_t*)malloc(sizeof(cand_t) * (size_t)(nc > 0 ? nc : 1));
     if (!s || !c) { free(s); free(c); return OR_ERR_SHAPE; }
     prefix_survival(conf, B, gamma, s);
-    double base = 0.0;
+    prog_t base = 0;
     for (int b = 0; b < B; ++b) base += progress(s + (int64_t)b * (gamma + 1), min_len);
     int64_t i = 0;
     for (int b = 0; b < B; ++b)
         for (int k = min_len + 1; k <= gamma; ++k) {
-            c[i].s = s[(int64_t)b * (gamma + 1) + k];
+            c[i].q = prog_quant(s[(int64_t)b * (gamma + 1) + k]);
             c[i].k = k;
             c[i].b = b;
             ++i;
@@ -453,7 +475,7 @@ static int sched_setup(const float* conf, int B, int gamma, int min_len, double*
 
 /* Exact scan: for every budget N from B(min_len+1) to B(gamma+1), the best
  * allocation keeps the top-(N - B(min_len+1)) candidates; tau(N) is the
- * sequential fp64 sum of the base and the sorted survivals, and the selected N
+ * fixed-point progress of the base and those candidates, and the selected N
  * is the first (smallest) strict maximum of tau(N) / C(N)
  * ([AS] eqs. (21), (23)-(24) with every budget a candidate).
  * out_gap: relative gap between the best objective and the best one at any
@@ -466,17 +488,17 @@ int oracle_sched_exact(const float* conf, int B, int gamma, const double* kt, co
     double* s;
     cand_t* c;
     int64_t nc;
-    double tau;
+    prog_t tau;
     st = sched_setup(conf, B, gamma, min_len, &s, &c, &nc, &tau);
     if (st != OR_OK) return st;
     double N0 = (double)B * (double)(min_len + 1);
-    double best = tau / cost_at(N0, kt, kc, nk);
+    double best = prog_value(tau) / cost_at(N0, kt, kc, nk);
     int64_t bestK = 0;
     double* objs = (double*)malloc(sizeof(double) * (size_t)(nc + 1));
     objs[0] = best;
     for (int64_t i = 0; i < nc; ++i) {
-        tau += c[i].s;
-        double obj = tau / cost_at(N0 + (double)(i + 1), kt, kc, nk);
+        tau += c[i].q;
+        double obj = prog_value(tau) / cost_at(N0 + (double)(i + 1), kt, kc, nk);
         objs[i + 1] = obj;
         if (obj > best) { best = obj; bestK = i + 1; }
     }
@@ -508,21 +530,21 @@ int oracle_sched_alg1(const float* conf, int B, int gamma, const double* kt, con
     double* s;
     cand_t* c;
     int64_t nc;
-    double tau;
+    prog_t tau;
     st = sched_setup(conf, B, gamma, min_len, &s, &c, &nc, &tau);
     if (st != OR_OK) return st;
     for (int b = 0; b < B; ++b) out_len[b] = min_len;
     double budget = (double)B * (double)(min_len + 1);
-    double theta_star = tau / cost_at(budget, kt, kc, nk);
+    double theta_star = prog_value(tau) / cost_at(budget, kt, kc, nk);
     const double eps = 0.0;
     for (int64_t i = 0; i < nc; ++i) {
-        if (!(c[i].s > eps)) continue; /* not a valid candidate */
+        if (!(prog_value(c[i].q) > eps)) continue; /* not a valid candidate */
         int r = c[i].b;
         if (out_len[r] != c[i].k - 1) continue; /* non-contiguous prefix: skip */
         out_len[r] = c[i].k;
         budget += 1.0;
-        tau += c[i].s;
-        double theta = tau / cost_at(budget, kt, kc, nk);
+        tau += c[i].q;
+        double theta = prog_value(tau) / cost_at(budget, kt, kc, nk);
         if (theta > theta_star) {
             theta_star = theta;
         } else {
@@ -554,13 +576,13 @@ int oracle_sched_brute(const float* conf, int B, int gamma, const double* kt, co
     double best = -INFINITY, second = -INFINITY;
     int64_t bestN = 0;
     for (;;) {
-        double tau = 0.0;
+        prog_t tau = 0;
         int64_t N = 0;
         for (int b = 0; b < B; ++b) {
             tau += progress(s + (int64_t)b * (gamma + 1), cur[b]);
             N += cur[b] + 1;
         }
-        double obj = tau / cost_at((double)N, kt, kc, nk);
+        double obj = prog_value(tau) / cost_at((double)N, kt, kc, nk);
         if (obj > best || (obj == best && N < bestN)) {
             if (best > second) second = best;
             best = obj;
@@ -584,8 +606,8 @@ int oracle_sched_brute(const float* conf, int B, int gamma, const double* kt, co
 /* D-cut ([AS] §4.2, eqs. (22)-(24)): the budget is restricted to the ratios
  * rho_i of the full verification budget B(gamma+1): K_i = max(B(min_len+1),
  * ceil(rho_i * B(gamma+1))); top-K_i selection (the same candidate order as
- * the exact scan) gives the estimated progress U_i = tau(K_i), summed left to
- * right in sorted order; the chosen ratio is the first maximum of U_i / C_i.
+ * the exact scan) gives the estimated progress U_i = tau(K_i) (fixed point,
+ * as for the exact scan); the chosen ratio is the first maximum of U_i / C_i.
  * ratios strictly increasing in (0, 1], costs positive. */
 int oracle_sched_dcut(const float* conf, int B, int gamma, const double* ratios, const double* costs, int nr,
                       int min_len, int32_t* out_len, int32_t* out_choice, double* out_obj) {
@@ -601,7 +623,7 @@ int oracle_sched_dcut(const float* conf, int B, int gamma, const double* ratios,
     double* s;
     cand_t* c;
     int64_t nc;
-    double base;
+    prog_t base;
     st = sched_setup(conf, B, gamma, min_len, &s, &c, &nc, &base);
     if (st != OR_OK) return st;
     const double N0 = (double)B * (double)(min_len + 1);
@@ -614,9 +636,9 @@ int oracle_sched_dcut(const float* conf, int B, int gamma, const double* ratios,
         if (K < N0) K = N0;
         if (K > Nmax) K = Nmax;
         const int64_t take = (int64_t)(K - N0);
-        double tau = base;
-        for (int64_t k = 0; k < take; ++k) tau += c[k].s;
-        const double obj = tau / costs[i];
+        prog_t tau = base;
+        for (int64_t k = 0; k < take; ++k) tau += c[k].q;
+        const double obj = prog_value(tau) / costs[i];
         if (out_obj) out_obj[i] = obj;
         if (obj > best) {
             best = obj;

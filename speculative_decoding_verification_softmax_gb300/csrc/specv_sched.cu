@@ -1,4 +1,5 @@
-// Confidence-scheduled verify lengths on GB300, one CTA per call.
+// Confidence-scheduled verify lengths on GB300: one thread-block cluster per
+// call for the batch schedulers, one warp per request for the static ones.
 //
 // Method (restated from the pages):
 //   * Prefix survival s_{b,0} = 1, s_{b,k} = prod_{t<=k} c_{b,t} ("AngelSpec"
@@ -12,17 +13,33 @@
 //     that budget; the call returns the allocation of the first N that
 //     maximises tau(N) / C(N) (eq. (24) with every budget a candidate), or,
 //     in Algorithm-1 mode ("UraionSpec" §3.5), stops at the first candidate
-//     that does not strictly improve tau / C.
+//     that does not strictly improve tau / C, or, in D-cut mode (§4.2,
+//     eqs. (22)-(24)), takes the best of the ratio budgets.
 //
-// All arithmetic is fp64 through explicit round-to-nearest intrinsics, in a
-// fixed order (products and sums left to right, tau summed sequentially in
-// sorted order), so the result is reproducible bit for bit.
+// Numbers.  Survival products are fp64, left to right.  Each survival is then
+// rounded to a multiple of 2^-46 and held as a 47-bit integer q: candidates
+// are ordered by q, and progress values are exact 64-bit integer sums of q, so
+// tau(N) does not depend on the order of summation and a parallel scan gives
+// the same bits as a sequential sum.  Objectives tau / C are fp64 through
+// explicit round-to-nearest intrinsics (no FMA contraction).
+//
+// GB300 has a narrow FP64 pipe, so the batch scheduler spreads its FP64 work
+// (survival products, STS powers, objectives) over the CTAs of a cluster;
+// the sort and the integer scan, which need no FP64, are repeated in every
+// CTA so that no further exchange is needed.
+#include <cooperative_groups.h>
 #include <math.h>
 #include <stdint.h>
 
 #include "specv_common.cuh"
 
+namespace cg = cooperative_groups;
+
 namespace specv {
+
+constexpr int kSchedThreads = 1024;
+constexpr int kSchedMaxCluster = 16;
+constexpr uint64_t kQField = (1ull << 47) - 1;  // survival field of a candidate key
 
 struct SchedArgs {
     const float* conf;
@@ -42,6 +59,18 @@ __device__ __forceinline__ double conf_at(const float* conf, const float* sts, i
     return has_sts ? pow(c, __ddiv_rn(1.0, (double)sts[k - 1])) : c;
 }
 
+// Survival s in [0, 1] as an integer multiple of 2^-46 (nearest, ties to even).
+__device__ __forceinline__ uint64_t surv_q(double s) { return __double2ull_rn(__dmul_rn(s, 0x1p46)); }
+
+// Progress value of an integer sum of survivals.
+__device__ __forceinline__ double prog_value(uint64_t t) { return __dmul_rn(__ull2double_rn(t), 0x1p-46); }
+
+// Candidate key, ascending = survival descending, then k, then b:
+// [63:17] complement of q, [16:12] k - 1, [11:0] b.
+__device__ __forceinline__ uint64_t cand_key(uint64_t q, int k, int b) {
+    return ((kQField - q) << 17) | ((uint64_t)(k - 1) << 12) | (uint64_t)b;
+}
+
 __device__ __forceinline__ double cost_at(double N, const SchedArgs& a) {
     if (N <= a.kt[0]) return a.kc[0];
     if (N >= a.kt[a.nk - 1]) return a.kc[a.nk - 1];
@@ -51,201 +80,315 @@ __device__ __forceinline__ double cost_at(double N, const SchedArgs& a) {
                                         __dsub_rn(a.kt[i + 1], a.kt[i])));
 }
 
-__global__ void __launch_bounds__(1024) k_schedule(SchedArgs a) {
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 15) & ~uintptr_t(15));
-    unsigned long long* key = (unsigned long long*)smem;          // [npad]; later tau / objectives
-    unsigned* id = (unsigned*)(key + a.npad);                    // [npad]
-    double* prog = (double*)(((uintptr_t)(id + a.npad) + 7) & ~uintptr_t(7));  // [B]; later counts
-    __shared__ int s_bad, s_npos, s_dcut_k;
-    __shared__ double s_base;
-    __shared__ double s_red_v[32];
-    __shared__ int s_red_i[32];
+// Bitonic compare-exchange stages with strides jmax..1 (all < 32) inside a warp.
+__device__ __forceinline__ uint64_t warp_bitonic(uint64_t v, int i, int k, int jmax) {
+    for (int j = jmax; j > 0; j >>= 1) {
+        const uint64_t p = __shfl_xor_sync(0xffffffffu, v, j);
+        const bool up = (i & k) == 0, low = (i & j) == 0;
+        v = (up == low) ? (v < p ? v : p) : (v < p ? p : v);
+    }
+    return v;
+}
 
-    const int tid = threadIdx.x, nt = blockDim.x;
-    const int B = a.B, G = a.gamma, ml = a.min_len, per = G - ml;
+// Largest value, ties to the smallest index (objectives are non-negative
+// doubles, so their bit patterns order like their values).
+__device__ __forceinline__ void warp_best(uint64_t& v, int& i) {
+    for (int o = 16; o > 0; o >>= 1) {
+        const uint64_t ov = __shfl_xor_sync(0xffffffffu, v, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+        if (ov > v || (ov == v && oi < i)) {
+            v = ov;
+            i = oi;
+        }
+    }
+}
+
+__device__ __forceinline__ uint64_t obj_bits(double v) { return (uint64_t)__double_as_longlong(v); }
+
+__global__ void __launch_bounds__(kSchedThreads, 1) k_schedule(SchedArgs a) {
+    cg::cluster_group cluster = cg::this_cluster();
+    const int CL = (int)cluster.num_blocks();
+    const int rank = (int)cluster.block_rank();
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    uint64_t* key = (uint64_t*)smem_raw;                 // [npad]: keys, then q, then tau; last: counts
+    uint16_t* cb = (uint16_t*)(key + a.npad);            // [npad]: request of each sorted candidate
+    double* stage = (double*)(cb + a.npad);              // [kSchedThreads]: confidences of one round
+    uint64_t* kst = (uint64_t*)(stage + kSchedThreads);  // [kSchedThreads]: keys of one round
+    __shared__ unsigned long long s_base_local;
+    __shared__ uint64_t s_base_part[kSchedMaxCluster];
+    __shared__ uint64_t s_slot_v[kSchedMaxCluster];
+    __shared__ int s_slot_i[kSchedMaxCluster];
+    __shared__ uint64_t s_red_v[32];
+    __shared__ int s_red_i[32];
+    __shared__ int s_bad, s_npos, s_bestK, s_dcut_k;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int B = a.B, G = a.gamma, ml = a.min_len, per = G - ml, nc = a.nc, npad = a.npad;
     if (tid == 0) {
         s_bad = 0;
-        *a.status = 0;
+        s_base_local = 0;
+        s_npos = 0;
     }
     __syncthreads();
-    for (int i = tid; i < B * G; i += nt) {
+    // every CTA checks the whole input, so that all take the same branch
+    for (int i = tid; i < B * G; i += kSchedThreads) {
         const float c = a.conf[i];
         if (!(c >= 0.0f && c <= 1.0f)) s_bad = 1;
     }
-    __syncthreads();
+    cluster.sync();  // also: every CTA runs before any shared-memory store across the cluster
     if (s_bad) {
-        for (int b = tid; b < B; b += nt) a.out[b] = -1;
-        if (tid == 0) *a.status = SPEC_ERR_CONFIDENCE;
+        if (rank == 0) {
+            for (int b = tid; b < B; b += kSchedThreads) a.out[b] = -1;
+            if (tid == 0) set_status(a.status, SPEC_ERR_CONFIDENCE);
+        }
+        return;
+    }
+    if (nc == 0) {
+        if (rank == 0)
+            for (int b = tid; b < B; b += kSchedThreads) a.out[b] = ml;
         return;
     }
 
-    // survival products, progress at min_len, candidate keys
-    for (int b = tid; b < B; b += nt) {
-        double s = 1.0, A = __dadd_rn(0.0, 1.0);
-        for (int k = 1; k <= G; ++k) {
-            s = __dmul_rn(s, conf_at(a.conf, a.sts, a.has_sts, (size_t)b * G + k - 1, k));
-            if (k <= ml) {
-                A = __dadd_rn(A, s);
-            } else {
-                const int ci = b * per + (k - ml - 1);
-                key[ci] = ~(unsigned long long)__double_as_longlong(s);
-                id[ci] = ((unsigned)k << 12) | (unsigned)b;
-            }
+    // 1. survivals of this CTA's requests, in rounds of kSchedThreads / G
+    //    requests; their keys go to every CTA of the cluster
+    const int bpc = (B + CL - 1) / CL;
+    const int b_lo = min(B, rank * bpc), b_hi = min(B, b_lo + bpc);
+    const int R = kSchedThreads / G;
+    for (int r0 = b_lo; r0 < b_hi; r0 += R) {
+        const int nr = min(R, b_hi - r0);
+        if (tid < nr * G) {
+            const int b = r0 + tid / G, k = tid % G + 1;
+            stage[tid] = conf_at(a.conf, a.sts, a.has_sts, (size_t)b * G + k - 1, k);
         }
-        prog[b] = A;
+        __syncthreads();
+        if (tid < nr) {
+            const int b = r0 + tid;
+            double s = 1.0;
+            uint64_t A = surv_q(1.0);  // k = 0
+            for (int k = 1; k <= G; ++k) {
+                s = __dmul_rn(s, stage[tid * G + k - 1]);
+                const uint64_t q = surv_q(s);
+                if (k <= ml)
+                    A += q;
+                else
+                    kst[tid * per + (k - ml - 1)] = cand_key(q, k, b);
+            }
+            atomicAdd(&s_base_local, (unsigned long long)A);
+        }
+        __syncthreads();
+        const int nkeys = nr * per;  // candidate index of kst[j] is r0 * per + j
+        for (int t = tid; t < nkeys * CL; t += kSchedThreads) {
+            const int j = t / CL, dst = t - j * CL;
+            *cluster.map_shared_rank(&key[r0 * per + j], dst) = kst[j];
+        }
+        __syncthreads();
     }
-    for (int i = a.nc + tid; i < a.npad; i += nt) {
-        key[i] = ~0ull;
-        id[i] = ~0u;
+    if (tid < CL) *cluster.map_shared_rank(&s_base_part[rank], tid) = (uint64_t)s_base_local;
+    for (int i = nc + tid; i < npad; i += kSchedThreads) key[i] = ~0ull;
+    cluster.sync();
+
+    uint64_t base = 0;
+    for (int r = 0; r < CL; ++r) base += s_base_part[r];
+
+    // 2. bitonic sort of the keys, ascending (every CTA); strides below 32 by
+    //    warp shuffles, the others through shared memory (npad >= 32, so the
+    //    threads of a warp are all in or all out)
+    for (int i = tid; i < npad; i += kSchedThreads) {
+        uint64_t v = key[i];
+        for (int k = 2; k <= 32 && k <= npad; k <<= 1) v = warp_bitonic(v, i, k, k >> 1);
+        key[i] = v;
     }
     __syncthreads();
-    if (tid == 0) {
-        double base = 0.0;
-        for (int b = 0; b < B; ++b) base = __dadd_rn(base, prog[b]);
-        s_base = base;
-    }
-
-    // bitonic sort ascending on (key, id): survival descending, then k, then b
-    for (int k = 2; k <= a.npad; k <<= 1) {
-        for (int j = k >> 1; j > 0; j >>= 1) {
+    for (int k = 64; k <= npad; k <<= 1) {
+        for (int j = k >> 1; j >= 32; j >>= 1) {
+            for (int p = tid; p < (npad >> 1); p += kSchedThreads) {
+                const int i = ((p & ~(j - 1)) << 1) | (p & (j - 1));
+                const uint64_t x = key[i], y = key[i + j];
+                if ((x > y) == ((i & k) == 0)) {
+                    key[i] = y;
+                    key[i + j] = x;
+                }
+            }
             __syncthreads();
-            for (int i = tid; i < a.npad; i += nt) {
-                const int p = i ^ j;
-                if (p > i) {
-                    const unsigned long long ki = key[i], kp = key[p];
-                    const unsigned ii = id[i], ip = id[p];
-                    const bool gt = ki > kp || (ki == kp && ii > ip);
-                    if (gt == ((i & k) == 0)) {
-                        key[i] = kp;
-                        key[p] = ki;
-                        id[i] = ip;
-                        id[p] = ii;
-                    }
-                }
-            }
         }
+        for (int i = tid; i < npad; i += kSchedThreads) key[i] = warp_bitonic(key[i], i, k, 16);
+        __syncthreads();
     }
+
+    // 3. survivals q in sorted order, the request of each, and the count of
+    //    positive ones (a prefix, q being descending)
+    int npos = 0;
+    for (int i = tid; i < npad; i += kSchedThreads) {
+        const uint64_t kk = key[i];
+        uint64_t q = 0;
+        if (i < nc) {
+            q = kQField - (kk >> 17);
+            cb[i] = (uint16_t)(kk & 4095u);
+        }
+        key[i] = q;
+        npos += q > 0;
+    }
+    for (int o = 16; o > 0; o >>= 1) npos += __shfl_xor_sync(0xffffffffu, npos, o);
+    if (lane == 0 && npos) atomicAdd(&s_npos, npos);
     __syncthreads();
 
-    // tau(N0 + i + 1) summed sequentially in sorted order
+    // 4. tau(K) = base + q_0 + ... + q_{K-1}, exact, in key[K-1]: each thread
+    //    scans a contiguous segment; segment totals by warp and block scans
+    {
+        const int E = npad > kSchedThreads ? npad / kSchedThreads : 1;
+        const bool has = tid * E < npad;
+        uint64_t run = 0;
+        if (has)
+            for (int e = 0; e < E; ++e) run += key[tid * E + e];
+        uint64_t incl = run;
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint64_t t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        if (lane == 31) s_red_v[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            const uint64_t w = s_red_v[lane];
+            uint64_t wi = w;
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint64_t t = __shfl_up_sync(0xffffffffu, wi, o);
+                if (lane >= o) wi += t;
+            }
+            s_red_v[lane] = wi - w;
+        }
+        __syncthreads();
+        uint64_t off = base + s_red_v[warp] + (incl - run);
+        if (has)
+            for (int e = 0; e < E; ++e) {
+                off += key[tid * E + e];
+                key[tid * E + e] = off;
+            }
+        __syncthreads();
+    }
+
+    // 5. objectives, split over the cluster
     const double N0 = __dmul_rn((double)B, (double)(ml + 1));
-    if (tid == 0) {
-        s_dcut_k = 0;
-        double tau = s_base;
-        int npos = a.nc;
-        for (int i = 0; i < a.nc; ++i) {
-            const double s = __longlong_as_double((long long)~key[i]);
-            if (npos == a.nc && !(s > 0.0)) npos = i;
-            tau = __dadd_rn(tau, s);
-            key[i] = (unsigned long long)__double_as_longlong(tau);
-        }
-        s_npos = npos;
-        if (a.mode == SPEC_SCHED_DCUT) {
-            // D-cut: tau at the budgets K_i = max(N0, ceil(rho_i * B(gamma+1))), first max of tau / C_i
-            const double Nmax = __dmul_rn((double)B, (double)(G + 1));
-            double best = -INFINITY;
-            int bestK = 0;
-            for (int i = 0; i < a.nk; ++i) {
-                double K = ceil(__dmul_rn(a.kt[i], Nmax));
-                if (K < N0) K = N0;
-                if (K > Nmax) K = Nmax;
-                const int take = (int)__dsub_rn(K, N0);
-                const double tau = take == 0 ? s_base : __longlong_as_double((long long)key[take - 1]);
-                const double obj = __ddiv_rn(tau, a.kc[i]);
-                if (obj > best) {
-                    best = obj;
-                    bestK = take;
-                }
-            }
-            s_dcut_k = bestK;
-        }
-    }
-    __syncthreads();
-    // objectives: obj(K) for K = 1..nc in key[K-1]; obj(0) from the base
-    for (int i = tid; i < a.nc; i += nt) {
-        const double tau = __longlong_as_double((long long)key[i]);
-        key[i] = (unsigned long long)__double_as_longlong(
-            __ddiv_rn(tau, cost_at(__dadd_rn(N0, (double)(i + 1)), a)));
-    }
-    __syncthreads();
-    const double obj0 = __ddiv_rn(s_base, cost_at(N0, a));
-    auto obj = [&](int K) -> double { return K == 0 ? obj0 : __longlong_as_double((long long)key[K - 1]); };
-
-    // pick K: exact = first maximum; Algorithm 1 = first non-improving valid candidate
-    double bv = -INFINITY;
+    auto tau_at = [&](int K) -> double { return prog_value(K == 0 ? base : key[K - 1]); };
+    auto obj_at = [&](int K) -> double { return __ddiv_rn(tau_at(K), cost_at(__dadd_rn(N0, (double)K), a)); };
+    uint64_t bv = 0;
     int bi = 0x7fffffff;
     if (a.mode == SPEC_SCHED_EXACT) {
-        for (int K = tid; K <= a.nc; K += nt) {
-            const double v = obj(K);
-            if (v > bv || (v == bv && K < bi)) { bv = v; bi = K; }
+        const int tot = nc + 1, cpc = (tot + CL - 1) / CL;
+        const int k_lo = min(tot, rank * cpc), k_hi = min(tot, k_lo + cpc);
+        for (int K = k_lo + tid; K < k_hi; K += kSchedThreads) {
+            const uint64_t v = obj_bits(obj_at(K));
+            if (v > bv || (v == bv && K < bi)) {
+                bv = v;
+                bi = K;
+            }
         }
-    } else {
-        bv = 0.0;
-        for (int i = tid; i < s_npos; i += nt)
-            if (!(obj(i + 1) > obj(i)) && i < bi) bi = i;
-        if (tid == 0 && s_npos < bi) bi = s_npos;
-    }
-    const int lane = tid & 31, warp = tid >> 5;
-    for (int o = 16; o > 0; o >>= 1) {
-        const double ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-    }
-    if (lane == 0) {
-        s_red_v[warp] = bv;
-        s_red_i[warp] = bi;
-    }
-    int* count = (int*)prog;
-    for (int b = tid; b < B; b += nt) count[b] = 0;
-    __syncthreads();
-    if (warp == 0) {
-        const int nw = nt >> 5;
-        bv = lane < nw ? s_red_v[lane] : -INFINITY;
-        bi = lane < nw ? s_red_i[lane] : 0x7fffffff;
-        for (int o = 16; o > 0; o >>= 1) {
-            const double ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+    } else if (a.mode == SPEC_SCHED_ALGORITHM1) {
+        // the first valid candidate i that does not strictly improve tau / C
+        const int np = s_npos, cpc = (np + CL - 1) / CL;
+        const int i_lo = min(np, rank * cpc), i_hi = min(np, i_lo + cpc);
+        for (int i = i_lo + tid; i < i_hi; i += kSchedThreads)
+            if (!(obj_at(i + 1) > obj_at(i)) && i < bi) bi = i;
+    } else if (rank == 0 && warp == 0) {
+        // D-cut: K_i = max(N0, ceil(rho_i * B(gamma+1))) for the nk ratios
+        const double Nmax = __dmul_rn((double)B, (double)(G + 1));
+        int take = 0;
+        if (lane < a.nk) {
+            double K = ceil(__dmul_rn(a.kt[lane], Nmax));
+            if (K < N0) K = N0;
+            if (K > Nmax) K = Nmax;
+            take = (int)__dsub_rn(K, N0);
+            bv = obj_bits(__ddiv_rn(tau_at(take), a.kc[lane]));
+            bi = lane;
         }
-        if (lane == 0) s_red_i[0] = bi;
+        warp_best(bv, bi);
+        const int take_best = __shfl_sync(0xffffffffu, take, bi & 31);
+        if (lane == 0) s_dcut_k = take_best;
+    }
+    if (a.mode != SPEC_SCHED_DCUT) {
+        if (a.mode == SPEC_SCHED_EXACT) {
+            warp_best(bv, bi);
+        } else {
+            for (int o = 16; o > 0; o >>= 1) bi = min(bi, __shfl_xor_sync(0xffffffffu, bi, o));
+        }
+        if (lane == 0) {
+            s_red_v[warp] = bv;
+            s_red_i[warp] = bi;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            bv = s_red_v[lane];
+            bi = s_red_i[lane];
+            if (a.mode == SPEC_SCHED_EXACT) {
+                warp_best(bv, bi);
+            } else {
+                for (int o = 16; o > 0; o >>= 1) bi = min(bi, __shfl_xor_sync(0xffffffffu, bi, o));
+            }
+            if (lane == 0) {
+                *cluster.map_shared_rank(&s_slot_v[rank], 0) = bv;
+                *cluster.map_shared_rank(&s_slot_i[rank], 0) = bi;
+            }
+        }
+    }
+    cluster.sync();
+    if (rank != 0) return;
+
+    // 6. rank 0: the chosen budget and the per-request counts
+    if (tid == 0) {
+        int bestK;
+        if (a.mode == SPEC_SCHED_DCUT) {
+            bestK = s_dcut_k;
+        } else if (a.mode == SPEC_SCHED_EXACT) {
+            uint64_t v = s_slot_v[0];
+            int k = s_slot_i[0];
+            for (int r = 1; r < CL; ++r)
+                if (s_slot_v[r] > v || (s_slot_v[r] == v && s_slot_i[r] < k)) {
+                    v = s_slot_v[r];
+                    k = s_slot_i[r];
+                }
+            bestK = k;
+        } else {
+            int k = s_npos;
+            for (int r = 0; r < CL; ++r) k = min(k, s_slot_i[r]);
+            bestK = k;
+        }
+        s_bestK = bestK;
     }
     __syncthreads();
-    const int bestK = a.mode == SPEC_SCHED_DCUT ? s_dcut_k : s_red_i[0];
-    for (int i = tid; i < bestK; i += nt) atomicAdd(&count[id[i] & 4095u], 1);
+    const int bestK = s_bestK;
+    int* count = (int*)key;  // tau is no longer needed
+    for (int b = tid; b < B; b += kSchedThreads) count[b] = 0;
     __syncthreads();
-    for (int b = tid; b < B; b += nt) a.out[b] = ml + count[b];
+    for (int i = tid; i < bestK; i += kSchedThreads) atomicAdd(&count[cb[i]], 1);
+    __syncthreads();
+    for (int b = tid; b < B; b += kSchedThreads) a.out[b] = ml + count[b];
 }
 
 // Static verify lengths: the leading positions whose (calibrated) confidence
-// is at least the threshold, clamped to [min_len, max_len].  One thread per
-// request.
-__global__ void k_schedule_static(const float* conf, int B, int G, double threshold, int max_len, int min_len,
-                                  int has_sts, SchedArgs sa, int32_t* out, int* status) {
-    const int b = blockIdx.x * blockDim.x + threadIdx.x;
-    if (b >= B) return;
-    int n = 0;
-    bool bad = false;
-    if (threshold <= 0.0) {
-        n = max_len;
-        if (conf)
-            for (int k = 0; k < G; ++k) {
-                const float c = conf[(size_t)b * G + k];
-                bad |= !(c >= 0.0f && c <= 1.0f);
-            }
-    } else {
-        for (int k = 0; k < G; ++k) {
-            const float c = conf[(size_t)b * G + k];
-            bad |= !(c >= 0.0f && c <= 1.0f);
+// is at least the threshold, clamped to [min_len, max_len].  One warp per
+// request, one lane per position; one warp per CTA spreads the fp64 powers of
+// STS over the SMs.
+__global__ void __launch_bounds__(32) k_schedule_static(const float* conf, int G, double threshold, int max_len,
+                                                        int min_len, int has_sts, SchedArgs sa, int32_t* out,
+                                                        int* status) {
+    const int b = blockIdx.x, lane = threadIdx.x;
+    bool bad = false, ok = true;
+    if (conf && lane < G) {
+        const float c = conf[(size_t)b * G + lane];
+        bad = !(c >= 0.0f && c <= 1.0f);
+        if (!bad && threshold > 0.0) ok = conf_at(conf, sa.sts, has_sts, (size_t)b * G + lane, lane + 1) >= threshold;
+    }
+    const unsigned badm = __ballot_sync(0xffffffffu, bad);
+    const unsigned okm = __ballot_sync(0xffffffffu, ok);
+    if (lane == 0) {
+        if (badm) {
+            out[b] = -1;
+            set_status(status, SPEC_ERR_CONFIDENCE);
+            return;
         }
-        while (!bad && n < max_len && conf_at(conf, sa.sts, has_sts, (size_t)b * G + n, n + 1) >= threshold) ++n;
+        int n = ~okm ? __ffs(~okm) - 1 : 32;
+        n = n < max_len ? n : max_len;
+        out[b] = n < min_len ? min_len : n;
     }
-    if (bad) {
-        out[b] = -1;
-        atomicCAS(status, 0, SPEC_ERR_CONFIDENCE);
-        return;
-    }
-    out[b] = n < min_len ? min_len : n;
 }
 
 }  // namespace specv
@@ -253,8 +396,50 @@ __global__ void k_schedule_static(const float* conf, int B, int G, double thresh
 using namespace specv;
 
 namespace {
-bool g_sched_attr[64];
+
+// Dynamic shared memory of k_schedule for a padded candidate count.
+size_t sched_smem_bytes(int npad) { return (size_t)npad * 10 + (size_t)kSchedThreads * 16 + 16; }
+
+// Cluster size of k_schedule per device: 16 CTAs where the GPU can place such
+// a cluster at the largest shared-memory size, else the portable 8; 0 = not
+// set up yet.
+int g_sched_cluster[64];
+
+int sched_cluster_size(int dev) {
+    if (g_sched_cluster[dev]) return g_sched_cluster[dev];
+    int npad_max = 32;
+    while (npad_max < SPEC_MAX_SCHED_CANDIDATES) npad_max <<= 1;
+    const size_t smem_max = sched_smem_bytes(npad_max);
+    if (cudaFuncSetAttribute((const void*)k_schedule, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem_max) != cudaSuccess)
+        return 0;
+    int cl = 8;
+    if (cudaFuncSetAttribute((const void*)k_schedule, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+        cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(kSchedMaxCluster);
+        cfg.blockDim = dim3(kSchedThreads);
+        cfg.dynamicSmemBytes = smem_max;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = kSchedMaxCluster;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, (const void*)k_schedule, &cfg) == cudaSuccess && n > 0)
+            cl = kSchedMaxCluster;
+        else
+            cudaGetLastError();
+    } else {
+        cudaGetLastError();
+    }
+    g_sched_cluster[dev] = cl;
+    return cl;
 }
+
+}  // namespace
 
 extern "C" {
 
@@ -302,7 +487,7 @@ int spec_schedule(const float* confidence, int B, int gamma, const spec_cost_tab
     a.mode = (int)mode;
     a.nk = cost->n;
     a.nc = B * (gamma - min_len);
-    int npad = 1;
+    int npad = 32;  // a power of two, at least one warp
     while (npad < a.nc) npad <<= 1;
     a.npad = npad;
     for (int i = 0; i < 32; ++i) {
@@ -311,17 +496,23 @@ int spec_schedule(const float* confidence, int B, int gamma, const spec_cost_tab
         a.sts[i] = (sts_temperature && i < gamma) ? sts_temperature[i] : 1.0f;
     }
     a.has_sts = sts_temperature ? 1 : 0;
-    const size_t smem = (size_t)npad * 12 + (size_t)B * 8 + 32;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPEC_ERR_CUDA;
-    if (!g_sched_attr[dev]) {
-        const int max_smem = SPEC_MAX_SCHED_CANDIDATES * 12 + SPEC_MAX_BATCH * 8 + 32;
-        if (cudaFuncSetAttribute((const void*)k_schedule, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 max_smem) != cudaSuccess)
-            return SPEC_ERR_CUDA;
-        g_sched_attr[dev] = true;
-    }
-    k_schedule<<<1, 1024, smem, (cudaStream_t)stream>>>(a);
+    const int cl = sched_cluster_size(dev);
+    if (!cl) return SPEC_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cl);
+    cfg.blockDim = dim3(kSchedThreads);
+    cfg.dynamicSmemBytes = sched_smem_bytes(npad);
+    cfg.stream = (cudaStream_t)stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, k_schedule, a) != cudaSuccess) return SPEC_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
@@ -340,12 +531,10 @@ int spec_schedule_static(const float* confidence, int B, int gamma, float thresh
     if (workspace_bytes < 256) return SPEC_ERR_WORKSPACE;
     SchedArgs sa;
     for (int i = 0; i < 32; ++i) sa.sts[i] = (sts_temperature && i < gamma) ? sts_temperature[i] : 1.0f;
-    // The status word is cleared before the launch: a block that finds a bad
-    // confidence may finish before any other block starts.
-    if (cudaMemsetAsync(workspace, 0, sizeof(int), (cudaStream_t)stream) != cudaSuccess) return SPEC_ERR_CUDA;
-    k_schedule_static<<<(B + 255) / 256, 256, 0, (cudaStream_t)stream>>>(
-        gamma > 0 ? confidence : nullptr, B, gamma, (double)threshold, max_len, min_len, sts_temperature ? 1 : 0, sa,
-        out_verify_len, (int*)workspace);
+    k_schedule_static<<<B, 32, 0, (cudaStream_t)stream>>>(gamma > 0 ? confidence : nullptr, gamma,
+                                                           (double)threshold, max_len, min_len,
+                                                           sts_temperature ? 1 : 0, sa, out_verify_len,
+                                                           (int*)workspace);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

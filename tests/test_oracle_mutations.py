@@ -49,6 +49,7 @@ MUTATIONS = {
     "threshold_strict": ("g_sts_T, n + 1) >= threshold) ++n;", "g_sts_T, n + 1) > threshold) ++n;"),
     "ece_no_abs": ("for (int k = 0; k < bins; ++k) e += fabs(sa[k] - sy[k]);",
                    "for (int k = 0; k < bins; ++k) e += sa[k] - sy[k];"),
+    "progress_coarse": ("#define PROG_FRAC_BITS 46", "#define PROG_FRAC_BITS 30"),
     "sts_power_inverted": ("a[i] = prefix[i] * pow((double)conf[(int64_t)i * gamma + k - 1], 1.0 / T);",
                            "a[i] = prefix[i] * pow((double)conf[(int64_t)i * gamma + k - 1], T);"),
 }

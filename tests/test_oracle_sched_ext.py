@@ -89,6 +89,39 @@ def test_dcut_matches_restricted_brute_force(min_len):
     assert checked > 200
 
 
+# ------------------------------------------------- progress accuracy
+def _exact_progress(conf, alloc):
+    """tau of an allocation in exact rational arithmetic from the fp32 confidences."""
+    from fractions import Fraction
+    tau = Fraction(0)
+    for b, ell in enumerate(alloc):
+        s = Fraction(1)
+        tau += s
+        for k in range(ell):
+            s *= Fraction(float(conf[b, k]))
+            tau += s
+    return tau
+
+
+@pytest.mark.parametrize("cost_name", ["Bprime", "C"])
+def test_objective_matches_exact_rational_progress(cost_name):
+    """The reported best objective equals the exact tau / C of the chosen
+    allocation to 1e-12 (relative): fp64 survival products plus survivals
+    rounded to 2^-46 lose far less than that at these sizes."""
+    from fractions import Fraction
+    cost = specsynth.COST_TABLES[cost_name]
+    rng = np.random.default_rng(12)
+    for trial in range(60):
+        B = int(rng.integers(1, 40))
+        gamma = int(rng.integers(1, 9))
+        conf = specsynth.make_confidences(B, gamma, seed=1300 + trial, mean=float(rng.uniform(-1, 3)))
+        r = oracle.sched_exact(conf, cost, 0)
+        alloc = r["verify_len"]
+        N = int((alloc + 1).sum())
+        exact = _exact_progress(conf, alloc) / Fraction(oracle.cost_at(N, cost))
+        assert abs(Fraction(r["obj"]) - exact) <= Fraction(1, 10 ** 12) * exact, trial
+
+
 # ---------------------------------------------------------- static modes
 def test_threshold_zero_is_fixed_length():
     """'A threshold of zero recovers standard fixed-length verification.'"""
