@@ -40,6 +40,7 @@ namespace specv {
 constexpr int kSchedThreads = 1024;
 constexpr int kSchedMaxCluster = 16;
 constexpr uint64_t kQField = (1ull << 47) - 1;  // survival field of a candidate key
+constexpr int kMergeMax = 4096;                 // candidates sorted by run merging
 
 struct SchedArgs {
     const float* conf;
@@ -59,11 +60,43 @@ __device__ __forceinline__ double conf_at(const float* conf, const float* sts, i
     return has_sts ? pow(c, __ddiv_rn(1.0, (double)sts[k - 1])) : c;
 }
 
-// Survival s in [0, 1] as an integer multiple of 2^-46 (nearest, ties to even).
-__device__ __forceinline__ uint64_t surv_q(double s) { return __double2ull_rn(__dmul_rn(s, 0x1p46)); }
+// Survival s in [0, 1] as an integer multiple of 2^-46, rounded to nearest
+// with ties to even.  Integer arithmetic on the bits of s: s = m * 2^(e-1075)
+// with a 53-bit m, so s * 2^46 = m >> (1029 - e) plus the rounding of the
+// bits shifted out (GB300's fp64 conversions are slow).
+__device__ __forceinline__ uint64_t surv_q(double s) {
+    const uint64_t bits = (uint64_t)__double_as_longlong(s);
+    const int e = (int)(bits >> 52);
+    if (e == 0) return 0;  // zero, or subnormal: far below 2^-47
+    const uint64_t m = (bits & ((1ull << 52) - 1)) | (1ull << 52);
+    const int sh = 1029 - e;  // >= 6 for s <= 1
+    if (sh >= 54) return 0;   // s * 2^46 < 1/2
+    const uint64_t q = m >> sh, rem = m & ((1ull << sh) - 1), half = 1ull << (sh - 1);
+    return q + ((rem > half || (rem == half && (q & 1))) ? 1 : 0);
+}
 
-// Progress value of an integer sum of survivals.
-__device__ __forceinline__ double prog_value(uint64_t t) { return __dmul_rn(__ull2double_rn(t), 0x1p-46); }
+// Progress value t * 2^-46 of an integer sum of survivals: the double
+// nearest to it (ties to even), built from the bits of t.
+__device__ __forceinline__ double prog_value(uint64_t t) {
+    if (t == 0) return 0.0;
+    int ex = 63 - __clzll((long long)t);
+    uint64_t m;
+    if (ex <= 52) {
+        m = t << (52 - ex);
+    } else {
+        const int sh = ex - 52;
+        m = t >> sh;
+        const uint64_t rem = t & ((1ull << sh) - 1), half = 1ull << (sh - 1);
+        if (rem > half || (rem == half && (m & 1))) {
+            ++m;
+            if (m >> 53) {
+                m >>= 1;
+                ++ex;
+            }
+        }
+    }
+    return __longlong_as_double((long long)(((uint64_t)(ex - 46 + 1023) << 52) | (m & ((1ull << 52) - 1))));
+}
 
 // Candidate key, ascending = survival descending, then k, then b:
 // [63:17] complement of q, [16:12] k - 1, [11:0] b.
@@ -105,6 +138,32 @@ __device__ __forceinline__ void warp_best(uint64_t& v, int& i) {
 
 __device__ __forceinline__ uint64_t obj_bits(double v) { return (uint64_t)__double_as_longlong(v); }
 
+// Number of entries of the ascending array a[0, n) below x (n >= 1):
+// branch-free binary search, the same trip count for every lane of a warp
+// searching arrays of one length.
+__device__ __forceinline__ int count_below(const uint64_t* a, int n, uint64_t x) {
+    int lo = 0;
+    for (int step = 1 << (31 - __clz(n)); step > 0; step >>= 1) {
+        const int t = lo + step;
+        if (t <= n && a[t - 1] < x) lo = t;
+    }
+    return lo;
+}
+
+// Split cluster barrier (PTX ISA, barrier.cluster): arrive without ordering
+// memory, wait later.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+
+// Outputs when there is nothing to schedule: every request invalid (bad
+// confidence), or no candidates (min_len == gamma).
+__device__ __forceinline__ void sched_trivial_out(const SchedArgs& a, bool bad, int tid) {
+    for (int b = tid; b < a.B; b += blockDim.x) a.out[b] = bad ? -1 : a.min_len;
+    if (bad && tid == 0) set_status(a.status, SPEC_ERR_CONFIDENCE);
+}
+
 __global__ void __launch_bounds__(kSchedThreads, 1) k_schedule(SchedArgs a) {
     cg::cluster_group cluster = cg::this_cluster();
     const int CL = (int)cluster.num_blocks();
@@ -124,95 +183,155 @@ __global__ void __launch_bounds__(kSchedThreads, 1) k_schedule(SchedArgs a) {
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int B = a.B, G = a.gamma, ml = a.min_len, per = G - ml, nc = a.nc, npad = a.npad;
+    // With STS the fp64 powers are split over the cluster and the keys are
+    // exchanged; without, every CTA computes every survival itself (a few
+    // fp64 products per request) and the cluster meets only at the end.
+    const bool split = a.has_sts != 0;
     if (tid == 0) {
         s_bad = 0;
         s_base_local = 0;
         s_npos = 0;
     }
+    if (!split) cluster_arrive_relaxed();  // waited on before the first store to another CTA
     __syncthreads();
-    // every CTA checks the whole input, so that all take the same branch
-    for (int i = tid; i < B * G; i += kSchedThreads) {
-        const float c = a.conf[i];
-        if (!(c >= 0.0f && c <= 1.0f)) s_bad = 1;
-    }
-    cluster.sync();  // also: every CTA runs before any shared-memory store across the cluster
-    if (s_bad) {
-        if (rank == 0) {
-            for (int b = tid; b < B; b += kSchedThreads) a.out[b] = -1;
-            if (tid == 0) set_status(a.status, SPEC_ERR_CONFIDENCE);
-        }
-        return;
-    }
-    if (nc == 0) {
-        if (rank == 0)
-            for (int b = tid; b < B; b += kSchedThreads) a.out[b] = ml;
-        return;
-    }
-
-    // 1. survivals of this CTA's requests, in rounds of kSchedThreads / G
-    //    requests; their keys go to every CTA of the cluster
-    const int bpc = (B + CL - 1) / CL;
-    const int b_lo = min(B, rank * bpc), b_hi = min(B, b_lo + bpc);
-    const int R = kSchedThreads / G;
-    for (int r0 = b_lo; r0 < b_hi; r0 += R) {
-        const int nr = min(R, b_hi - r0);
-        if (tid < nr * G) {
-            const int b = r0 + tid / G, k = tid % G + 1;
-            stage[tid] = conf_at(a.conf, a.sts, a.has_sts, (size_t)b * G + k - 1, k);
-        }
-        __syncthreads();
-        if (tid < nr) {
-            const int b = r0 + tid;
-            double s = 1.0;
-            uint64_t A = surv_q(1.0);  // k = 0
-            for (int k = 1; k <= G; ++k) {
-                s = __dmul_rn(s, stage[tid * G + k - 1]);
-                const uint64_t q = surv_q(s);
-                if (k <= ml)
-                    A += q;
-                else
-                    kst[tid * per + (k - ml - 1)] = cand_key(q, k, b);
-            }
-            atomicAdd(&s_base_local, (unsigned long long)A);
-        }
-        __syncthreads();
-        const int nkeys = nr * per;  // candidate index of kst[j] is r0 * per + j
-        for (int t = tid; t < nkeys * CL; t += kSchedThreads) {
-            const int j = t / CL, dst = t - j * CL;
-            *cluster.map_shared_rank(&key[r0 * per + j], dst) = kst[j];
-        }
-        __syncthreads();
-    }
-    if (tid < CL) *cluster.map_shared_rank(&s_base_part[rank], tid) = (uint64_t)s_base_local;
-    for (int i = nc + tid; i < npad; i += kSchedThreads) key[i] = ~0ull;
-    cluster.sync();
 
     uint64_t base = 0;
-    for (int r = 0; r < CL; ++r) base += s_base_part[r];
-
-    // 2. bitonic sort of the keys, ascending (every CTA); strides below 32 by
-    //    warp shuffles, the others through shared memory (npad >= 32, so the
-    //    threads of a warp are all in or all out)
-    for (int i = tid; i < npad; i += kSchedThreads) {
-        uint64_t v = key[i];
-        for (int k = 2; k <= 32 && k <= npad; k <<= 1) v = warp_bitonic(v, i, k, k >> 1);
-        key[i] = v;
+    if (split) {
+        // every CTA checks the whole input, so that all take the same branch
+        for (int i = tid; i < B * G; i += kSchedThreads) {
+            const float c = a.conf[i];
+            if (!(c >= 0.0f && c <= 1.0f)) s_bad = 1;
+        }
+        cluster.sync();  // also: every CTA runs before any shared-memory store across the cluster
+        if (s_bad || nc == 0) {
+            if (rank == 0) sched_trivial_out(a, s_bad != 0, tid);
+            return;
+        }
     }
-    __syncthreads();
-    for (int k = 64; k <= npad; k <<= 1) {
-        for (int j = k >> 1; j >= 32; j >>= 1) {
-            for (int p = tid; p < (npad >> 1); p += kSchedThreads) {
-                const int i = ((p & ~(j - 1)) << 1) | (p & (j - 1));
-                const uint64_t x = key[i], y = key[i + j];
-                if ((x > y) == ((i & k) == 0)) {
-                    key[i] = y;
-                    key[i + j] = x;
+
+    // 1. survivals in rounds of kSchedThreads / G requests: the round's
+    //    (calibrated) confidences staged in shared memory by all threads, then
+    //    one thread per request takes the products.  Split: this CTA's share
+    //    of the requests, keys sent to every CTA; else all requests, checking
+    //    the confidences on the way.
+    {
+        const int bpc = split ? (B + CL - 1) / CL : B;
+        const int b_lo = min(B, rank * (split ? bpc : 0)), b_hi = min(B, b_lo + bpc);
+        const int R = kSchedThreads / max(G, 1);
+        for (int r0 = b_lo; r0 < b_hi; r0 += R) {
+            const int nr = min(R, b_hi - r0);
+            if (tid < nr * G) {
+                const int b = r0 + tid / G, k = tid - (tid / G) * G + 1;
+                const size_t i = (size_t)b * G + k - 1;
+                double c;
+                if (split) {
+                    c = conf_at(a.conf, a.sts, 1, i, k);
+                } else {
+                    const float cf = a.conf[i];
+                    if (!(cf >= 0.0f && cf <= 1.0f)) s_bad = 1;
+                    c = (cf >= 0.0f && cf <= 1.0f) ? (double)cf : 0.0;
+                }
+                stage[tid] = c;
+            }
+            __syncthreads();
+            if (tid < ((nr + 31) & ~31)) {  // whole warps, for the sum below
+                uint64_t A = 0;
+                if (tid < nr) {
+                    const int b = r0 + tid;
+                    uint64_t* dst = split ? kst + tid * per : key + (size_t)b * per;
+                    double s = 1.0;
+                    A = surv_q(1.0);  // k = 0
+                    for (int k = 1; k <= G; ++k) {
+                        s = __dmul_rn(s, stage[tid * G + k - 1]);
+                        const uint64_t q = surv_q(s);
+                        if (k <= ml)
+                            A += q;
+                        else
+                            dst[k - ml - 1] = cand_key(q, k, b);
+                    }
+                }
+                for (int o = 16; o > 0; o >>= 1) A += __shfl_xor_sync(0xffffffffu, A, o);
+                if (lane == 0 && A) atomicAdd(&s_base_local, (unsigned long long)A);
+            }
+            __syncthreads();
+            if (split) {
+                const int nkeys = nr * per;  // candidate index of kst[j] is r0 * per + j
+                for (int t = tid; t < nkeys * CL; t += kSchedThreads) {
+                    const int j = t / CL, dst = t - j * CL;
+                    *cluster.map_shared_rank(&key[r0 * per + j], dst) = kst[j];
+                }
+                __syncthreads();
+            }
+        }
+    }
+    for (int i = nc + tid; i < npad; i += kSchedThreads) key[i] = ~0ull;
+    if (split) {
+        if (tid < CL) *cluster.map_shared_rank(&s_base_part[rank], tid) = (uint64_t)s_base_local;
+        cluster.sync();
+        for (int r = 0; r < CL; ++r) base += s_base_part[r];
+    } else {
+        __syncthreads();
+        if (s_bad || nc == 0) {
+            cluster_wait();
+            if (rank == 0) sched_trivial_out(a, s_bad != 0, tid);
+            return;
+        }
+        base = s_base_local;
+    }
+
+    // 2. sort the keys ascending (every CTA).  Each request's keys already
+    //    form an ascending run of `per`; up to kMergeMax candidates the runs
+    //    are merged pairwise, each key moving to its own index plus its
+    //    rank in the partner run; above that, a bitonic network.
+    if (nc <= kMergeMax) {
+        for (int L = per; L < nc; L <<= 1) {
+            uint64_t xv[kMergeMax / kSchedThreads];
+            int np[kMergeMax / kSchedThreads];
+#pragma unroll
+            for (int e = 0; e < kMergeMax / kSchedThreads; ++e) {
+                const int i = tid + e * kSchedThreads;
+                if (i < nc) {
+                    const uint64_t x = key[i];
+                    const int m = i / L, own = i - m * L;
+                    const int lo = (m ^ 1) * L, hi = min(nc, lo + L);
+                    const int cnt = lo < nc ? count_below(key + lo, hi - lo, x) : 0;
+                    xv[e] = x;
+                    np[e] = (m & ~1) * L + own + cnt;
                 }
             }
             __syncthreads();
+#pragma unroll
+            for (int e = 0; e < kMergeMax / kSchedThreads; ++e) {
+                const int i = tid + e * kSchedThreads;
+                if (i < nc) key[np[e]] = xv[e];
+            }
+            __syncthreads();
         }
-        for (int i = tid; i < npad; i += kSchedThreads) key[i] = warp_bitonic(key[i], i, k, 16);
+    } else {
+        // bitonic: strides below 32 by warp shuffles, the others through
+        // shared memory (npad >= 32, so the threads of a warp are all in or
+        // all out)
+        for (int i = tid; i < npad; i += kSchedThreads) {
+            uint64_t v = key[i];
+            for (int k = 2; k <= 32 && k <= npad; k <<= 1) v = warp_bitonic(v, i, k, k >> 1);
+            key[i] = v;
+        }
         __syncthreads();
+        for (int k = 64; k <= npad; k <<= 1) {
+            for (int j = k >> 1; j >= 32; j >>= 1) {
+                for (int p = tid; p < (npad >> 1); p += kSchedThreads) {
+                    const int i = ((p & ~(j - 1)) << 1) | (p & (j - 1));
+                    const uint64_t x = key[i], y = key[i + j];
+                    if ((x > y) == ((i & k) == 0)) {
+                        key[i] = y;
+                        key[i + j] = x;
+                    }
+                }
+                __syncthreads();
+            }
+            for (int i = tid; i < npad; i += kSchedThreads) key[i] = warp_bitonic(key[i], i, k, 16);
+            __syncthreads();
+        }
     }
 
     // 3. survivals q in sorted order, the request of each, and the count of
@@ -304,6 +423,7 @@ __global__ void __launch_bounds__(kSchedThreads, 1) k_schedule(SchedArgs a) {
         const int take_best = __shfl_sync(0xffffffffu, take, bi & 31);
         if (lane == 0) s_dcut_k = take_best;
     }
+    if (!split) cluster_wait();  // every CTA of the cluster runs
     if (a.mode != SPEC_SCHED_DCUT) {
         if (a.mode == SPEC_SCHED_EXACT) {
             warp_best(bv, bi);
