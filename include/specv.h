@@ -71,7 +71,8 @@ enum {
     SPEC_ERR_TIMEOUT = -10,    /* device: a bounded wait expired (results of the call invalid) */
     SPEC_ERR_CUDA = -11,       /* a CUDA runtime call failed (launch, attribute query) */
     SPEC_ERR_UNIFORM = -12,    /* device: a used uniform outside [0, 1) */
-    SPEC_ERR_CONFIDENCE = -13  /* device: a confidence outside [0, 1] or NaN */
+    SPEC_ERR_CONFIDENCE = -13, /* device: a confidence outside [0, 1] or NaN */
+    SPEC_ERR_ROW_INDEX = -14   /* device: packed rows of a request outside the packed arrays */
 };
 
 /* Limits of this build. */
@@ -119,6 +120,44 @@ int spec_verify(const void* target_logits, const void* draft_logits, spec_dtype 
                 float temperature, const float* uniforms, int32_t* out_tokens,
                 int32_t* out_accept_len, void* workspace, size_t workspace_bytes,
                 spec_stream_t stream);
+
+/*
+ * Verification on packed logits ("AngelSpec" §4.2, "Packing and correctness":
+ * after the budget is chosen, the unequal request prefixes are packed into one
+ * dense verification batch and only those positions reach the target model).
+ * Same method, outputs, workspace and errors as spec_verify; only where the
+ * logit rows live differs:
+ *   target_logits  [K_target, V], dt: request b's target rows 0..ell_b are rows
+ *                  target_row[b] .. target_row[b] + ell_b.
+ *   draft_logits   [K_draft, V], dt: request b's draft rows 0..ell_b-1 are rows
+ *                  draft_row[b] .. draft_row[b] + ell_b - 1 (not read when
+ *                  temperature == 0; may then be NULL, as may draft_row).
+ *   target_row, draft_row  [B] int32 device arrays (the row index).  Any
+ *                  placement is allowed (dense request-major packing is what
+ *                  spec_pack_rows writes); a request whose rows fall outside
+ *                  [0, K) is marked invalid with SPEC_ERR_ROW_INDEX and none of
+ *                  its rows are read.
+ *   verify_len     [B] int32 as for spec_verify (NULL: gamma for all).
+ * Fixed launch shapes for given (B, gamma, V, dt, temperature), no host
+ * synchronisation: capturable in a CUDA graph, one per batch shape.
+ */
+int spec_verify_packed(const void* target_logits, int K_target, const void* draft_logits, int K_draft,
+                       const int32_t* target_row, const int32_t* draft_row, spec_dtype dt, int B,
+                       int gamma, int V, const int32_t* draft_tokens, const int32_t* verify_len,
+                       float temperature, const float* uniforms, int32_t* out_tokens,
+                       int32_t* out_accept_len, void* workspace, size_t workspace_bytes,
+                       spec_stream_t stream);
+
+/*
+ * Dense request-major packing of ragged prefixes (the layout of the packed
+ * batch in "AngelSpec" §4.2): from verify_len [B] (device), writes
+ *   target_row[b] = sum_{b' < b} (ell_b' + 1),   draft_row[b] = sum_{b' < b} ell_b',
+ *   totals[0] = K_target = sum_b (ell_b + 1),    totals[1] = K_draft = sum_b ell_b
+ * (all device int32; a verify length outside [0, gamma] counts as no rows).
+ * One launch, no host synchronisation.  Requires B <= 4096.
+ */
+int spec_pack_rows(const int32_t* verify_len, int B, int gamma, int32_t* target_row, int32_t* draft_row,
+                   int32_t* totals, spec_stream_t stream);
 
 /*
  * Diagnostics of the last spec_verify that used `workspace` (same B, gamma, V,

@@ -120,6 +120,17 @@ def verify_probs(P, Q, tokens, uniforms) -> dict:
     return out
 
 
+def pack_rows(verify_len, gamma: int) -> dict:
+    """Dense request-major row index of ragged prefixes."""
+    vl = np.ascontiguousarray(verify_len, np.int32)
+    B = vl.shape[0]
+    tr = np.empty(B, np.int32)
+    dr = np.empty(B, np.int32)
+    tot = np.empty(2, np.int32)
+    rc = _L().oracle_pack_rows(_p(vl), B, gamma, _p(tr), _p(dr), _p(tot))
+    return dict(rc=rc, target_row=tr, draft_row=dr, K_target=int(tot[0]), K_draft=int(tot[1]))
+
+
 def _knots(cost):
     kt = np.ascontiguousarray(cost[0], np.float64)
     kc = np.ascontiguousarray(cost[1], np.float64)

@@ -348,6 +348,29 @@ int oracle_verify_probs(const double* P, const double* Q, int B, int gamma, int 
     return OR_OK;
 }
 
+/* Dense packing of ragged prefixes ([AS] §4.2, "Packing and correctness": the
+ * kept prefixes form one dense verification batch).  Request-major order:
+ * request b's ell_b + 1 target rows follow those of requests 0..b-1, and so do
+ * its ell_b draft rows; a verify length outside [0, gamma] contributes no rows.
+ * Writes the first row of every request and the two row totals. */
+int oracle_pack_rows(const int32_t* verify_len, int B, int gamma, int32_t* target_row, int32_t* draft_row,
+                     int32_t* totals) {
+    if (B < 0 || gamma < 0) return OR_ERR_SHAPE;
+    int32_t t = 0, d = 0;
+    for (int b = 0; b < B; ++b) {
+        target_row[b] = t;
+        draft_row[b] = d;
+        const int ell = verify_len[b];
+        if (ell >= 0 && ell <= gamma) {
+            t += ell + 1;
+            d += ell;
+        }
+    }
+    totals[0] = t;
+    totals[1] = d;
+    return OR_OK;
+}
+
 /* ----------------------------------------------------------------- scheduler */
 
 /* Piecewise-linear round cost C(N): knots (t_i, c_i) with strictly increasing

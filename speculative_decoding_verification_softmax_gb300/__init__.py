@@ -26,6 +26,7 @@ NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3", 
 OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_TEMPERATURE = 0, -1, -2, -3, -4
 ERR_VERIFY_LEN, ERR_TOKEN, ERR_WORKSPACE, ERR_COST_TABLE = -5, -6, -7, -8
 ERR_NONFINITE, ERR_TIMEOUT, ERR_CUDA, ERR_UNIFORM, ERR_CONFIDENCE = -9, -10, -11, -12, -13
+ERR_ROW_INDEX = -14
 F32, BF16 = 0, 1
 SCHED_EXACT, SCHED_ALGORITHM1, SCHED_DCUT = 0, 1, 2
 MAX_BATCH, MAX_GAMMA, MAX_SCHED_CANDIDATES = 4096, 32, 16384
@@ -33,7 +34,8 @@ MAX_BATCH, MAX_GAMMA, MAX_SCHED_CANDIDATES = 4096, 32, 16384
 EXPORTED = ["spec_verify_workspace_bytes", "spec_verify", "spec_verify_stats",
             "spec_schedule_workspace_bytes", "spec_schedule", "spec_read_status",
             "spec_status_string", "spec_profile_events", "spec_verify_kernel_count",
-            "spec_verify_static", "spec_schedule_static", "spec_sts_fit"]
+            "spec_verify_static", "spec_schedule_static", "spec_sts_fit", "spec_verify_packed",
+            "spec_pack_rows"]
 STATIC_WORKSPACE_BYTES = 8 << 20
 
 
@@ -120,6 +122,11 @@ def lib():
                 L.spec_verify_kernel_count.restype = i32
                 L.spec_verify_static.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, f32, vp, vp, vp, vp]
                 L.spec_verify_static.restype = i32
+                L.spec_verify_packed.argtypes = [vp, i32, vp, i32, vp, vp, i32, i32, i32, i32, vp, vp, f32, vp,
+                                                 vp, vp, vp, sz, vp]
+                L.spec_verify_packed.restype = i32
+                L.spec_pack_rows.argtypes = [vp, i32, i32, vp, vp, vp, vp]
+                L.spec_pack_rows.restype = i32
                 _lib = L
     return _lib
 
@@ -249,6 +256,61 @@ def verify_static(target_logits, draft_logits, draft_tokens, verify_len, tempera
                                   _ptr(out_tokens), _ptr(out_accept_len), _stream_handle(stream))
     _check(rc, "spec_verify_static")
     return out_tokens, out_accept_len
+
+
+def verify_packed(target_logits, draft_logits, target_row, draft_row, draft_tokens, verify_len,
+                  temperature: float, uniforms, *, out_tokens=None, out_accept_len=None, workspace=None,
+                  stream=None):
+    """Run spec_verify_packed: target_logits [K_target, V] and draft_logits
+    [K_draft, V] (bf16 or fp32, contiguous; draft may be None at temperature 0),
+    the row index target_row / draft_row [B] int32, draft_tokens [B, gamma]
+    int32, verify_len [B] int32 or None, uniforms [B, gamma+2] fp32.
+    Returns (out_tokens [B, gamma+1], out_accept_len [B], workspace)."""
+    torch = _torch()
+    Kt, V = target_logits.shape
+    B, gamma = draft_tokens.shape
+    Kd = draft_logits.shape[0] if draft_logits is not None else 0
+    dt = _dtype_code(target_logits)
+    dev = target_logits.device
+    for name, t in (("target_logits", target_logits), ("draft_logits", draft_logits), ("target_row", target_row),
+                    ("draft_row", draft_row), ("draft_tokens", draft_tokens), ("verify_len", verify_len),
+                    ("uniforms", uniforms)):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if draft_logits is not None and (draft_logits.dtype != target_logits.dtype or draft_logits.shape[1] != V):
+        raise TypeError("draft_logits must have the dtype and vocabulary of target_logits")
+    if out_tokens is None:
+        out_tokens = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
+    if out_accept_len is None:
+        out_accept_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = alloc_verify_workspace(B, gamma, V, dt, dev)
+    rc = lib().spec_verify_packed(_ptr(target_logits), Kt, _ptr(draft_logits), Kd, _ptr(target_row),
+                                  _ptr(draft_row), dt, B, gamma, V, _ptr(draft_tokens), _ptr(verify_len),
+                                  ctypes.c_float(temperature), _ptr(uniforms), _ptr(out_tokens),
+                                  _ptr(out_accept_len), _ptr(workspace), workspace.numel(),
+                                  _stream_handle(stream))
+    _check(rc, "spec_verify_packed")
+    return out_tokens, out_accept_len, workspace
+
+
+def pack_rows(verify_len, gamma: int, *, target_row=None, draft_row=None, totals=None, stream=None):
+    """Run spec_pack_rows on verify_len [B] int32 (CUDA): the dense request-major
+    row index.  Returns (target_row [B], draft_row [B], totals [2] = (K_target,
+    K_draft)), all int32 on the device."""
+    torch = _torch()
+    B = verify_len.shape[0]
+    dev = verify_len.device
+    if target_row is None:
+        target_row = torch.empty((B,), dtype=torch.int32, device=dev)
+    if draft_row is None:
+        draft_row = torch.empty((B,), dtype=torch.int32, device=dev)
+    if totals is None:
+        totals = torch.empty((2,), dtype=torch.int32, device=dev)
+    rc = lib().spec_pack_rows(_ptr(verify_len), B, gamma, _ptr(target_row), _ptr(draft_row), _ptr(totals),
+                              _stream_handle(stream))
+    _check(rc, "spec_pack_rows")
+    return target_row, draft_row, totals
 
 
 def verify_stats(workspace, B: int, gamma: int, V: int, dtype_code: int, stream=None):

@@ -75,6 +75,7 @@ const char* spec_status_string(int status) {
         case SPEC_ERR_CUDA: return "CUDA runtime error";
         case SPEC_ERR_UNIFORM: return "a used uniform is outside [0, 1)";
         case SPEC_ERR_CONFIDENCE: return "a confidence is outside [0, 1]";
+        case SPEC_ERR_ROW_INDEX: return "packed rows of a request lie outside the packed arrays";
         default: return "unknown status";
     }
 }

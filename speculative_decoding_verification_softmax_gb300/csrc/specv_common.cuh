@@ -244,6 +244,38 @@ __device__ __forceinline__ float scaled_exp(float z, float c_hi, float c_lo, flo
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Where the logit rows of a request live.  Padded layout (trow == nullptr):
+// target row (b, j) is row b*(gamma+1) + j of the target array and draft row
+// (b, j) is row b*gamma + j of the draft array.  Packed layout: rows
+// trow[b] + j of a [Kt, V] target array and drow[b] + j of a [Kd, V] draft
+// array.
+struct RowMap {
+    const int32_t* trow;
+    const int32_t* drow;
+    int Kt, Kd;
+};
+
+__device__ __forceinline__ size_t target_row(const RowMap& m, int b, int j, int G1) {
+    return m.trow ? (size_t)(m.trow[b] + j) : (size_t)b * G1 + j;
+}
+
+__device__ __forceinline__ size_t draft_row(const RowMap& m, int b, int j, int G) {
+    return m.drow ? (size_t)(m.drow[b] + j) : (size_t)b * G + j;
+}
+
+// True when the rows request b reads (target 0..ell, draft 0..ell-1 if
+// `draft`) lie inside the packed arrays; always true for the padded layout.
+__device__ __forceinline__ bool rows_in_range(const RowMap& m, int b, int ell, bool draft) {
+    if (!m.trow) return true;
+    const int t = m.trow[b];
+    bool ok = t >= 0 && t <= m.Kt - ell - 1;
+    if (draft && ell > 0) {
+        const int d = m.drow[b];
+        ok = ok && d >= 0 && d <= m.Kd - ell;
+    }
+    return ok;
+}
+
 __device__ __forceinline__ void set_status(int* status_word, int err) {
     atomicCAS(status_word, 0, err);
 }

@@ -53,14 +53,17 @@ struct StatsArgs {
     int B, gamma, V;
     float c_hi, c_lo;
     char* ws;
+    RowMap rm;
 };
 
 // Rows a request needs: target 0..ell and (T > 0) draft 0..ell-1; 0 when
-// verify_len is out of range (the accept kernel marks the request invalid).
+// verify_len is out of range or packed rows fall outside the packed arrays
+// (the finish kernel marks the request invalid).
 template <bool GREEDY>
-__device__ __forceinline__ int rows_of(const int32_t* verify_len, int b, int gamma) {
+__device__ __forceinline__ int rows_of(const int32_t* verify_len, const RowMap& rm, int b, int gamma) {
     const int ell = verify_len ? verify_len[b] : gamma;
     if (ell < 0 || ell > gamma) return 0;
+    if (!rows_in_range(rm, b, ell, !GREEDY)) return 0;
     return GREEDY ? ell + 1 : 2 * ell + 1;
 }
 
@@ -74,7 +77,8 @@ __device__ __forceinline__ int row_id(int b, int k, int cnt, int gamma, int T1) 
 // prefix[b] = rows of requests < b, prefix[B] = total; table[r] = global row id
 // of compact row r when the total fits.  Whole CTA.
 template <bool GREEDY>
-__device__ void block_row_plan(const int32_t* verify_len, int B, int gamma, int* prefix, int* table) {
+__device__ void block_row_plan(const int32_t* verify_len, const RowMap& rm, int B, int gamma, int* prefix,
+                               int* table) {
     __shared__ int s_w[32];
     __shared__ int s_total;
     constexpr int PER = (SPEC_MAX_BATCH + kStatsThreads - 1) / kStatsThreads;
@@ -84,7 +88,7 @@ __device__ void block_row_plan(const int32_t* verify_len, int B, int gamma, int*
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
         const int b = tid * PER + i;
-        cnt[i] = b < B ? rows_of<GREEDY>(verify_len, b, gamma) : 0;
+        cnt[i] = b < B ? rows_of<GREEDY>(verify_len, rm, b, gamma) : 0;
         mine += cnt[i];
     }
     int incl = mine;
@@ -273,7 +277,7 @@ __global__ void __launch_bounds__(kStatsThreads, 1) k_row_stats(StatsArgs a, Lay
         for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
         fence_mbar_init();
     }
-    block_row_plan<GREEDY>(a.verify_len, a.B, a.gamma, prefix, table);
+    block_row_plan<GREEDY>(a.verify_len, a.rm, a.B, a.gamma, prefix, table);
     __syncthreads();
     pdl_trigger();
 
@@ -308,7 +312,13 @@ __global__ void __launch_bounds__(kStatsThreads, 1) k_row_stats(StatsArgs a, Lay
         return row_id<GREEDY>(k.b, k.r - prefix[k.b], cnt, a.gamma, T1);
     };
     auto row_ptr = [&](int g) -> const char* {
-        return g < T1 ? a.target + (size_t)g * a.V * ES : a.draft + (size_t)(g - T1) * a.V * ES;
+        if (!a.rm.trow) return g < T1 ? a.target + (size_t)g * a.V * ES : a.draft + (size_t)(g - T1) * a.V * ES;
+        if (g < T1) {
+            const int b = g / (a.gamma + 1);
+            return a.target + target_row(a.rm, b, g - b * (a.gamma + 1), a.gamma + 1) * a.V * ES;
+        }
+        const int gd = g - T1, b = gd / a.gamma;
+        return a.draft + draft_row(a.rm, b, gd - b * a.gamma, a.gamma) * a.V * ES;
     };
 
     Cursor ic{gw / nch, gw - (gw / nch) * nch, 0};  // issue cursor

@@ -456,6 +456,7 @@ struct FinishArgs {
     int B, gamma, V;
     float c_hi, c_lo;
     char* ws;
+    RowMap rm;
 };
 
 struct RowStatS {
@@ -494,7 +495,9 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
     const float2* partial = (const float2*)(a.ws + L.partial);
     const int G1 = a.gamma + 1, T1 = a.B * G1;
     const int ell = a.verify_len ? a.verify_len[b] : a.gamma;
+    // rows_ok: the request's rows exist (the streaming kernel read them)
     const bool ell_ok = ell >= 0 && ell <= a.gamma;
+    const bool rows_ok = ell_ok && rows_in_range(a.rm, b, ell, !GREEDY);
 
     // 1. caller inputs only (ready before the streaming kernel started)
     int st = SPEC_OK;
@@ -502,6 +505,7 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
     float uj = 0.f, ug = 0.f, ub = 0.f;
     if (warp == 0) {
         if (!ell_ok) st = SPEC_ERR_VERIFY_LEN;
+        else if (!rows_ok) st = SPEC_ERR_ROW_INDEX;
         const int j = lane;
         if (ell_ok && j < ell) x = a.tokens[(size_t)b * a.gamma + j];
         if (!GREEDY && ell_ok) {
@@ -511,10 +515,10 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
             ub = u[a.gamma + 1];
         }
         const bool xok = x >= 0 && x < a.V;
-        if (!GREEDY && ell_ok && j < ell) {
+        if (!GREEDY && rows_ok && j < ell) {
             const int xc = xok ? x : 0;
-            s_zt[j] = load_logit<ES>(a.target + (size_t)(b * G1 + j) * a.V * ES, xc);
-            s_zd[j] = load_logit<ES>(a.draft + (size_t)(b * a.gamma + j) * a.V * ES, xc);
+            s_zt[j] = load_logit<ES>(a.target + target_row(a.rm, b, j, G1) * a.V * ES, xc);
+            s_zd[j] = load_logit<ES>(a.draft + draft_row(a.rm, b, j, a.gamma) * a.V * ES, xc);
         }
         if (st == SPEC_OK && !__all_sync(0xffffffffu, xok)) st = SPEC_ERR_TOKEN;
         if (st == SPEC_OK && !GREEDY) {
@@ -528,7 +532,7 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
     const bool timed_out = warp == 0 && hdr[kHdrStatus] == SPEC_ERR_TIMEOUT;
 
     // 2. row merges: target rows 0..ell, then draft rows 0..ell-1
-    const int nrows = ell_ok ? (GREEDY ? ell + 1 : 2 * ell + 1) : 0;
+    const int nrows = rows_ok ? (GREEDY ? ell + 1 : 2 * ell + 1) : 0;
     for (int r = gw; r < nrows; r += nw) {
         const int g = r <= ell ? b * G1 + r : T1 + b * a.gamma + (r - ell - 1);
         RowStatS rs;
@@ -630,8 +634,8 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
     if (job.status != SPEC_OK) return;  // the same in every CTA of the cluster
 
     // 4. residual sums per chunk and per lane segment over the cluster's warps
-    const char* rt = a.target + (size_t)job.g_t * a.V * ES;
-    const char* rd = job.mode == 1 ? a.draft + (size_t)(job.g_d - T1) * a.V * ES : rt;
+    const char* rt = a.target + target_row(a.rm, b, job.n, G1) * a.V * ES;
+    const char* rd = job.mode == 1 ? a.draft + draft_row(a.rm, b, job.n, a.gamma) * a.V * ES : rt;
     float* rchunk = (float*)(a.ws + L.rchunk) + (size_t)b * L.nch;
     const bool tot_smem = L.nch <= kChunkSmem;
     const bool round_smem = L.nch <= kRoundSmem;
@@ -747,6 +751,72 @@ __global__ void k_copy_stats(const char* ws, Layout L, int B, int gamma, double*
     }
 }
 
+// Dense request-major packing of the rows of ragged prefixes: exclusive
+// prefix sums of ell_b + 1 (target rows) and ell_b (draft rows).  One CTA.
+constexpr int kPackThreads = 1024;
+
+__global__ void __launch_bounds__(kPackThreads) k_pack_rows(const int32_t* verify_len, int B, int gamma,
+                                                            int32_t* trow, int32_t* drow, int32_t* totals) {
+    __shared__ int s_t[32], s_d[32];
+    constexpr int PER = (SPEC_MAX_BATCH + kPackThreads - 1) / kPackThreads;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int ct[PER], cd[PER], mt = 0, md = 0;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int b = tid * PER + i;
+        const int ell = b < B ? verify_len[b] : -1;
+        const bool ok = ell >= 0 && ell <= gamma;
+        ct[i] = ok ? ell + 1 : 0;
+        cd[i] = ok ? ell : 0;
+        mt += ct[i];
+        md += cd[i];
+    }
+    int it = mt, id = md;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int vt = __shfl_up_sync(0xffffffffu, it, o), vd = __shfl_up_sync(0xffffffffu, id, o);
+        if (lane >= o) {
+            it += vt;
+            id += vd;
+        }
+    }
+    if (lane == 31) {
+        s_t[warp] = it;
+        s_d[warp] = id;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int wt = s_t[lane], wd = s_d[lane];
+        int xt = wt, xd = wd;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int vt = __shfl_up_sync(0xffffffffu, xt, o), vd = __shfl_up_sync(0xffffffffu, xd, o);
+            if (lane >= o) {
+                xt += vt;
+                xd += vd;
+            }
+        }
+        s_t[lane] = xt - wt;
+        s_d[lane] = xd - wd;
+        if (lane == 31) {
+            totals[0] = xt;
+            totals[1] = xd;
+        }
+    }
+    __syncthreads();
+    int ot = s_t[warp] + it - mt, od = s_d[warp] + id - md;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int b = tid * PER + i;
+        if (b < B) {
+            trow[b] = ot;
+            drow[b] = od;
+        }
+        ot += ct[i];
+        od += cd[i];
+    }
+}
+
 }  // namespace specv
 
 // ===================================================================== host
@@ -826,17 +896,8 @@ int launch_chain(const StatsArgs& sa, const FinishArgs& fa, const Layout& L, int
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
-}  // namespace
-
-extern "C" {
-
-size_t spec_verify_workspace_bytes(int B, int gamma, int V, spec_dtype dt) {
-    if (check_shape(B, gamma, V, dt) != SPEC_OK) return 0;
-    return Layout(B, gamma, V, dt == SPEC_BF16 ? 2 : 4).total;
-}
-
-int spec_verify(const void* target_logits, const void* draft_logits, spec_dtype dt, int B, int gamma,
-                int V, const int32_t* draft_tokens, const int32_t* verify_len, float temperature,
+int verify_impl(const void* target_logits, const void* draft_logits, const RowMap& rm, spec_dtype dt, int B,
+                int gamma, int V, const int32_t* draft_tokens, const int32_t* verify_len, float temperature,
                 const float* uniforms, int32_t* out_tokens, int32_t* out_accept_len, void* workspace,
                 size_t workspace_bytes, spec_stream_t stream) {
     int rc = check_shape(B, gamma, V, dt);
@@ -870,15 +931,62 @@ int spec_verify(const void* target_logits, const void* draft_logits, spec_dtype 
     const char* t = (const char*)target_logits;
     const char* d = (const char*)draft_logits;
     char* ws = (char*)workspace;
-    StatsArgs sa{t, d, verify_len, B, gamma, V, c_hi, c_lo, ws};
-    FinishArgs fa{t, d, draft_tokens, verify_len, uniforms, out_tokens, out_accept_len, B, gamma, V, c_hi, c_lo, ws};
+    StatsArgs sa{t, d, verify_len, B, gamma, V, c_hi, c_lo, ws, rm};
+    FinishArgs fa{t,     d,     draft_tokens, verify_len, uniforms, out_tokens, out_accept_len, B, gamma, V,
+                  c_hi, c_lo, ws,           rm};
     cudaStream_t st = (cudaStream_t)stream;
     // every row starts on a 16-byte boundary: whole-chunk copies
-    const bool al = aligned(target_logits, 16) && (greedy || gamma == 0 || aligned(draft_logits, 16)) &&
+    const bool al = aligned(target_logits, 16) && (greedy || gamma == 0 || !draft_logits || aligned(draft_logits, 16)) &&
                     ((size_t)V * es) % 16 == 0;
     if (es == 2)
         return greedy ? launch_chain<2, true>(sa, fa, L, sms, al, st) : launch_chain<2, false>(sa, fa, L, sms, al, st);
     return greedy ? launch_chain<4, true>(sa, fa, L, sms, al, st) : launch_chain<4, false>(sa, fa, L, sms, al, st);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t spec_verify_workspace_bytes(int B, int gamma, int V, spec_dtype dt) {
+    if (check_shape(B, gamma, V, dt) != SPEC_OK) return 0;
+    return Layout(B, gamma, V, dt == SPEC_BF16 ? 2 : 4).total;
+}
+
+int spec_verify(const void* target_logits, const void* draft_logits, spec_dtype dt, int B, int gamma,
+                int V, const int32_t* draft_tokens, const int32_t* verify_len, float temperature,
+                const float* uniforms, int32_t* out_tokens, int32_t* out_accept_len, void* workspace,
+                size_t workspace_bytes, spec_stream_t stream) {
+    return verify_impl(target_logits, draft_logits, RowMap{nullptr, nullptr, 0, 0}, dt, B, gamma, V, draft_tokens,
+                       verify_len, temperature, uniforms, out_tokens, out_accept_len, workspace, workspace_bytes,
+                       stream);
+}
+
+int spec_verify_packed(const void* target_logits, int K_target, const void* draft_logits, int K_draft,
+                       const int32_t* target_row, const int32_t* draft_row, spec_dtype dt, int B, int gamma, int V,
+                       const int32_t* draft_tokens, const int32_t* verify_len, float temperature,
+                       const float* uniforms, int32_t* out_tokens, int32_t* out_accept_len, void* workspace,
+                       size_t workspace_bytes, spec_stream_t stream) {
+    if (K_target < 0 || K_draft < 0) return SPEC_ERR_SHAPE;
+    if (B > 0) {
+        if (!target_row) return SPEC_ERR_NULL;
+        if (temperature != 0.0f && gamma > 0 && !draft_row) return SPEC_ERR_NULL;
+        if (!aligned(target_row, 4) || (draft_row && !aligned(draft_row, 4))) return SPEC_ERR_ALIGN;
+    }
+    return verify_impl(target_logits, draft_logits, RowMap{target_row, draft_row, K_target, K_draft}, dt, B, gamma,
+                       V, draft_tokens, verify_len, temperature, uniforms, out_tokens, out_accept_len, workspace,
+                       workspace_bytes, stream);
+}
+
+int spec_pack_rows(const int32_t* verify_len, int B, int gamma, int32_t* target_row, int32_t* draft_row,
+                   int32_t* totals, spec_stream_t stream) {
+    if (B < 0 || B > SPEC_MAX_BATCH || gamma < 0 || gamma > SPEC_MAX_GAMMA) return SPEC_ERR_SHAPE;
+    if (!totals) return SPEC_ERR_NULL;
+    if (B > 0 && (!verify_len || !target_row || !draft_row)) return SPEC_ERR_NULL;
+    if (!aligned(totals, 4) || (verify_len && !aligned(verify_len, 4)) || (target_row && !aligned(target_row, 4)) ||
+        (draft_row && !aligned(draft_row, 4)))
+        return SPEC_ERR_ALIGN;
+    k_pack_rows<<<1, kPackThreads, 0, (cudaStream_t)stream>>>(verify_len, B, gamma, target_row, draft_row, totals);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
 int spec_verify_stats(const void* workspace, size_t workspace_bytes, int B, int gamma, int V,

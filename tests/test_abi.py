@@ -130,8 +130,31 @@ def test_schedule_rejects_bad_temperatures(L):
         assert L.spec_schedule(FAKE, 4, 4, ctypes.byref(table), 0, 0, T, FAKE, FAKE, 256, None) == sv.ERR_SHAPE
 
 
+def test_verify_packed_host_errors(L):
+    def vp(B=4, gamma=4, V=1024, Kt=20, Kd=16, trow=FAKE, drow=FAKE, T=1.0, ws_bytes=1 << 40, **kw):
+        return L.spec_verify_packed(kw.get("target", FAKE), Kt, kw.get("draft", FAKE), Kd, trow, drow, sv.F32, B,
+                                    gamma, V, FAKE, None, ctypes.c_float(T), FAKE, FAKE, FAKE, FAKE, ws_bytes, None)
+
+    assert vp(Kt=-1) == sv.ERR_SHAPE
+    assert vp(trow=None) == sv.ERR_NULL
+    assert vp(drow=None) == sv.ERR_NULL
+    assert vp(drow=None, T=0.0, ws_bytes=16) == sv.ERR_WORKSPACE     # greedy reads no draft rows
+    assert vp(trow=ctypes.c_void_p(0x10002)) == sv.ERR_ALIGN
+    assert vp(B=4097) == sv.ERR_SHAPE
+    assert vp(ws_bytes=16) == sv.ERR_WORKSPACE
+    assert vp(B=0, trow=None, drow=None, target=None, draft=None) == sv.OK
+
+
+def test_pack_rows_host_errors(L):
+    assert L.spec_pack_rows(FAKE, 4097, 4, FAKE, FAKE, FAKE, None) == sv.ERR_SHAPE
+    assert L.spec_pack_rows(FAKE, 4, 33, FAKE, FAKE, FAKE, None) == sv.ERR_SHAPE
+    assert L.spec_pack_rows(None, 4, 4, FAKE, FAKE, FAKE, None) == sv.ERR_NULL
+    assert L.spec_pack_rows(FAKE, 4, 4, FAKE, FAKE, None, None) == sv.ERR_NULL
+    assert L.spec_pack_rows(FAKE, 4, 4, ctypes.c_void_p(0x10001), FAKE, FAKE, None) == sv.ERR_ALIGN
+
+
 def test_status_strings(L):
-    for code in range(-13, 1):
+    for code in range(-14, 1):
         assert sv.status_string(code) and "unknown" not in sv.status_string(code)
     assert "unknown" in sv.status_string(-99)
 

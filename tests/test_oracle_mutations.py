@@ -49,6 +49,8 @@ MUTATIONS = {
     "threshold_strict": ("g_sts_T, n + 1) >= threshold) ++n;", "g_sts_T, n + 1) > threshold) ++n;"),
     "ece_no_abs": ("for (int k = 0; k < bins; ++k) e += fabs(sa[k] - sy[k]);",
                    "for (int k = 0; k < bins; ++k) e += sa[k] - sy[k];"),
+    "pack_rows_inclusive": ("        target_row[b] = t;\n        draft_row[b] = d;\n        const int ell = verify_len[b];\n        if (ell >= 0 && ell <= gamma) {\n            t += ell + 1;\n            d += ell;\n        }",
+                            "        const int ell = verify_len[b];\n        if (ell >= 0 && ell <= gamma) {\n            t += ell + 1;\n            d += ell;\n        }\n        target_row[b] = t;\n        draft_row[b] = d;"),
     "progress_coarse": ("#define PROG_FRAC_BITS 46", "#define PROG_FRAC_BITS 30"),
     "sts_power_inverted": ("a[i] = prefix[i] * pow((double)conf[(int64_t)i * gamma + k - 1], 1.0 / T);",
                            "a[i] = prefix[i] * pow((double)conf[(int64_t)i * gamma + k - 1], T);"),
@@ -70,6 +72,7 @@ def test_pins_catch_planted_mistake(name, tmp_path):
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_verify.py"),
                         os.path.join(ROOT, "tests", "test_oracle_sched.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_sched_ext.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_sched_ext.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_pack.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"pins did not catch mutation {name}:\n{r.stdout[-2000:]}"
