@@ -3,7 +3,10 @@
 Default workload: block-diffusion verification, B=64 requests per GPU,
 gamma=16 draft tokens, V=131072, bf16 logits, T=1 (synthetic, seeded).  One
 step = one spec_verify call over the whole batch (plan, row statistics,
-accept / first rejection, residual or bonus draw).
+accept / first rejection, residual or bonus draw).  The JSON line also carries
+the schedulers' per-call device times, a schedule-then-verify step on the
+scheduled ragged workload, and the same step with D-cut, dense packing and
+packed verification.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -268,6 +271,65 @@ def time_schedulers(sv, dev, stream, rank: int):
             "kernel_launches_per_call": 1, "modes": res}
 
 
+def time_packed_step(sv, specsynth, case, t, d, x, u, dev, stream, rank: int, steps: int):
+    """D-cut budget, dense packing and verification on packed logits: the
+    deployed path of the scheduled workload.  The ratio costs C(B, rho) are the
+    round-cost table at the budgets K_rho; the packed logits are gathered once
+    from the padded batch (what the target model would write), outside the
+    timed region."""
+    import math
+    import torch
+    B, gamma, V = case.B, case.gamma, case.V
+    conf = torch.from_numpy(specsynth.make_confidences(seed=specsynth.SCHED_SEED + 1000 * rank)).to(dev)
+    kt, kc = specsynth.COST_TABLES["Bprime"]
+    ratios = [0.25, 0.5, 0.75, 1.0]
+    budgets = [max(B, math.ceil(r * B * (gamma + 1))) for r in ratios]
+    costs = [float(np.interp(k, kt, kc)) for k in budgets]
+    vl = torch.empty((B,), dtype=torch.int32, device=dev)
+    sws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    tr = torch.empty((B,), dtype=torch.int32, device=dev)
+    dr = torch.empty((B,), dtype=torch.int32, device=dev)
+    tot = torch.empty((2,), dtype=torch.int32, device=dev)
+    sv.schedule(conf, (ratios, costs), 0, sv.SCHED_DCUT, out_verify_len=vl, workspace=sws)
+    sv.pack_rows(vl, gamma, target_row=tr, draft_row=dr, totals=tot)
+    torch.cuda.synchronize(dev)
+    vl_h, tr_h, dr_h = vl.cpu().numpy(), tr.cpu().numpy(), dr.cpu().numpy()
+    Kt, Kd = (int(v) for v in tot.cpu().numpy())
+    ti = np.concatenate([b * (gamma + 1) + np.arange(vl_h[b] + 1) for b in range(B)])
+    di = np.concatenate([b * gamma + np.arange(vl_h[b]) for b in range(B)])
+    tp = t.view(B * (gamma + 1), V)[torch.from_numpy(ti).to(dev)].contiguous()
+    dp = d.view(B * gamma, V)[torch.from_numpy(di).to(dev)].contiguous()
+    assert (tr_h == np.concatenate([[0], np.cumsum(vl_h + 1)[:-1]])).all()
+    out_t = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
+    out_n = torch.empty((B,), dtype=torch.int32, device=dev)
+    ws = sv.alloc_verify_workspace(B, gamma, V, sv.BF16, dev)
+
+    def step():
+        sv.schedule(conf, (ratios, costs), 0, sv.SCHED_DCUT, out_verify_len=vl, workspace=sws)
+        sv.pack_rows(vl, gamma, target_row=tr, draft_row=dr, totals=tot)
+        sv.verify_packed(tp, dp, tr, dr, x, vl, case.T, u, out_tokens=out_t, out_accept_len=out_n, workspace=ws)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    if sv.read_status(ws) != 0 or sv.read_status(sws) != 0:
+        raise RuntimeError("device status on the packed step")
+    rows = int(vl_h.sum())
+    logit_bytes = (Kt + Kd) * V * 2
+    return {"workload": "D-cut budget (ratios 0.25..1, costs = the round-cost table at K_rho), dense packing, "
+                        f"verify of the {WORKLOAD} logits packed as [{Kt}, V] target and [{Kd}, V] draft rows",
+            "ms_per_step": ms, "verified_rows_per_step": rows, "verified_rows_per_s": rows / (ms / 1e3),
+            "packed_logit_bytes": logit_bytes, "logit_gbs": logit_bytes / (ms / 1e3) / 1e9,
+            "steps": steps, "kernel_launches_per_step": 2 + sv.kernel_count(B, case.T)}
+
+
 def run_ours(args):
     import torch
     import specsynth
@@ -368,6 +430,7 @@ def run_ours(args):
                       "verified_rows_per_s": s_rows / (s_ms / 1e3), "steps": s_steps,
                       "kernel_launches_per_step": 1 + sv.kernel_count(B, case.T)}
     sched = time_schedulers(sv, dev, stream, rank)
+    packed_step = time_packed_step(sv, specsynth, case, t, d, x, u, dev, stream, rank, s_steps)
 
     # end to end through the public API: pinned host inputs -> device -> verify -> host outputs
     h_t = torch.from_numpy(case.target.view(np.int16)).pin_memory()
@@ -438,6 +501,7 @@ def run_ours(args):
         "device_status": status,
         "scheduled_step": scheduled_step,
         "schedule": sched,
+        "scheduled_step_packed": packed_step,
         "mean_accept_len": float(n.mean()),
     }
     print(json.dumps(line), flush=True)
@@ -466,11 +530,35 @@ def run_profile_case(args):
         raise SystemExit(1)
 
 
+def run_profile_sched(args):
+    """A case for ncu captures of the scheduler: spec_schedule (exact scan, cost
+    table B', min_len 1) on the scheduled workload's 64 x 16 confidences, a few
+    calls, nothing else."""
+    import torch
+    import specsynth
+    import speculative_decoding_verification_softmax_gb300 as sv
+    sv.build()
+    conf = torch.from_numpy(specsynth.make_confidences()).cuda()
+    out = torch.empty((conf.shape[0],), dtype=torch.int32, device="cuda")
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup + args.steps):
+        sv.schedule(conf, specsynth.COST_TABLES["Bprime"], specsynth.SCHED_MIN_LEN, sv.SCHED_EXACT,
+                    out_verify_len=out, workspace=ws)
+    torch.cuda.synchronize()
+    st = sv.read_status(ws)
+    print(json.dumps({"profile_sched": "scheduled ragged", "calls": args.warmup + args.steps, "status": st,
+                      "verified_rows": int(out.sum().item())}))
+    if st != 0:
+        raise SystemExit(1)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--profile-case", action="store_true",
                     help="run only a small case for ncu (B=--profile-batch)")
     ap.add_argument("--profile-batch", type=int, default=24)
+    ap.add_argument("--profile-sched", action="store_true",
+                    help="run only the scheduler on the scheduled workload (for ncu)")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
@@ -478,6 +566,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.profile_case:
         run_profile_case(args)
+    elif args.profile_sched:
+        run_profile_sched(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -208,9 +208,15 @@ size_t spec_schedule_workspace_bytes(int B, int gamma);
  *                   Scaling ("UraionSpec" §2.4): the scheduler uses the calibrated
  *                   confidence c_{b,k}^(1/T_k) (fp64 pow) in place of c_{b,k}.
  *   out_verify_len  [B] int32 in [min_len, gamma] (all -1 if a confidence is invalid).
- * Arithmetic is fp64 with a fixed order (left-to-right products and sums, the
- * budget prefix summed in sorted order), so results are reproducible bit for
- * bit.  Requires B <= 4096, gamma <= 32, B * (gamma - min_len) <= 16384.
+ * Numbers: survival products are fp64, left to right; each survival is then
+ * rounded to a multiple of 2^-46 (nearest, ties to even).  Candidates are
+ * ordered by that value (ties: shallower position, then lower request) and
+ * progress values are exact integer sums of it, so tau(N) does not depend on
+ * the order of summation; objectives tau / C are fp64 with explicit rounding.
+ * Results are reproducible bit for bit.  The status word in `workspace` is
+ * sticky: set on an error, cleared by spec_read_status (zero the workspace
+ * once before first use).  Requires B <= 4096, gamma <= 32,
+ * B * (gamma - min_len) <= 16384.  One thread-block cluster per call.
  */
 int spec_schedule(const float* confidence, int B, int gamma, const spec_cost_table* cost,
                   int min_len, spec_sched_mode mode, const float* sts_temperature,
