@@ -74,11 +74,10 @@ __device__ __forceinline__ int row_id(int b, int k, int cnt, int gamma, int T1) 
     return k <= ell ? b * (gamma + 1) + k : T1 + b * gamma + (k - ell - 1);
 }
 
-// prefix[b] = rows of requests < b, prefix[B] = total; table[r] = global row id
-// of compact row r when the total fits.  Whole CTA.
+// prefix[b] = rows of requests < b, prefix[B] = total.  Whole CTA; ends
+// with a barrier, so every thread sees the prefix.
 template <bool GREEDY>
-__device__ void block_row_plan(const int32_t* verify_len, const RowMap& rm, int B, int gamma, int* prefix,
-                               int* table) {
+__device__ void block_row_prefix(const int32_t* verify_len, const RowMap& rm, int B, int gamma, int* prefix) {
     __shared__ int s_w[32];
     __shared__ int s_total;
     constexpr int PER = (SPEC_MAX_BATCH + kStatsThreads - 1) / kStatsThreads;
@@ -120,19 +119,30 @@ __device__ void block_row_plan(const int32_t* verify_len, const RowMap& rm, int 
         off += cnt[i];
     }
     if (tid == 0) prefix[B] = total;
-    if (total > kTableRows) return;
     __syncthreads();
-    // table[r]: request of compact row r by binary search over the prefix
+}
+
+// table[r] = global row id of compact row r (when the total fits): one warp
+// per request writes its rows.  No barrier inside.
+template <bool GREEDY>
+__device__ void block_row_table(const int* prefix, int B, int gamma, int* table) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int T1 = B * (gamma + 1);
-    for (int r = tid; r < total; r += kStatsThreads) {
-        int lo = 0, hi = B - 1;  // largest b with prefix[b] <= r
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (prefix[mid] <= r) lo = mid;
-            else hi = mid - 1;
-        }
-        table[r] = row_id<GREEDY>(lo, r - prefix[lo], prefix[lo + 1] - prefix[lo], gamma, T1);
+    for (int b = warp; b < B; b += kStatsWarps) {
+        const int p0 = prefix[b], cnt = prefix[b + 1] - p0;
+        for (int k = lane; k < cnt; k += 32) table[p0 + k] = row_id<GREEDY>(b, k, cnt, gamma, T1);
     }
+}
+
+// The request owning compact row r: the largest b with prefix[b] <= r.
+__device__ __forceinline__ int request_of_row(const int* prefix, int B, int r) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (prefix[mid] <= r) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
 }
 
 // Statistics of one chunk: nvec 16-byte vectors in shared memory holding the
@@ -277,20 +287,22 @@ __global__ void __launch_bounds__(kStatsThreads, 1) k_row_stats(StatsArgs a, Lay
         for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
         fence_mbar_init();
     }
-    block_row_plan<GREEDY>(a.verify_len, a.rm, a.B, a.gamma, prefix, table);
-    __syncthreads();
+    block_row_prefix<GREEDY>(a.verify_len, a.rm, a.B, a.gamma, prefix);
     pdl_trigger();
 
     const int nch = L.nch;
     const int n_rows = prefix[a.B];
     const long long total = (long long)n_rows * nch;
     const int W = gridDim.x * kStatsWarps;
-    const int gw = blockIdx.x * kStatsWarps + warp;
-    if (gw >= total) return;
-    const long long count = (total - gw + W - 1) / W;  // items of this warp
+    // warps numbered across the grid (local warp index major), so that the
+    // items left over by W not dividing the total spread over every SM
+    const int gw = warp * gridDim.x + blockIdx.x;
+    const bool has_items = gw < total;
+    const long long count = has_items ? (total - gw + W - 1) / W : 0;  // items of this warp
     const int Wq = W / nch, Wr = W - Wq * nch;
     const int T1 = a.B * (a.gamma + 1);
     const bool use_table = n_rows <= kTableRows;
+    bool table_ready = false;  // the first copies are issued before the table is built
 
     // A cursor over this warp's items: (compact row, chunk) and the request
     // of the row (for the prefix walk when the table does not fit).
@@ -306,7 +318,7 @@ __global__ void __launch_bounds__(kStatsThreads, 1) k_row_stats(StatsArgs a, Lay
         }
     };
     auto row_of = [&](Cursor& k) -> int {
-        if (use_table) return table[k.r];
+        if (table_ready) return table[k.r];
         while (prefix[k.b + 1] <= k.r) ++k.b;
         const int cnt = prefix[k.b + 1] - prefix[k.b];
         return row_id<GREEDY>(k.b, k.r - prefix[k.b], cnt, a.gamma, T1);
@@ -322,7 +334,8 @@ __global__ void __launch_bounds__(kStatsThreads, 1) k_row_stats(StatsArgs a, Lay
     };
 
     Cursor ic{gw / nch, gw - (gw / nch) * nch, 0};  // issue cursor
-    Cursor cc = ic;                                   // consume cursor
+    if (has_items) ic.b = request_of_row(prefix, a.B, ic.r);
+    Cursor cc = ic;  // consume cursor
     uint32_t pending = 0;  // bit s: a copy is in flight on stage s
     uint32_t phase = 0;    // bit s: parity of the next wait on stage s
     long long issued = 0;
@@ -363,6 +376,13 @@ __global__ void __launch_bounds__(kStatsThreads, 1) k_row_stats(StatsArgs a, Lay
 
 #pragma unroll 1
     for (int s = 0; s < kStages && issued < count; ++s) issue(s);
+    // the row table is built while those copies are in flight
+    if (use_table) {
+        block_row_table<GREEDY>(prefix, a.B, a.gamma, table);
+        __syncthreads();
+        table_ready = true;
+    }
+    if (!has_items) return;
     __syncwarp();
 
     int s = 0;
