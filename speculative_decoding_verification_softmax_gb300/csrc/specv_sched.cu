@@ -40,7 +40,7 @@ namespace specv {
 constexpr int kSchedThreads = 1024;
 constexpr int kSchedMaxCluster = 16;
 constexpr uint64_t kQField = (1ull << 47) - 1;  // survival field of a candidate key
-constexpr int kMergeMax = 4096;                 // candidates sorted by run merging
+constexpr int kRankMax = 4096;                  // candidates ordered by distributed ranking
 
 struct SchedArgs {
     const float* conf;
@@ -173,6 +173,7 @@ __global__ void __launch_bounds__(kSchedThreads, 1) k_schedule(SchedArgs a) {
     uint16_t* cb = (uint16_t*)(key + a.npad);            // [npad]: request of each sorted candidate
     double* stage = (double*)(cb + a.npad);              // [kSchedThreads]: confidences of one round
     uint64_t* kst = (uint64_t*)(stage + kSchedThreads);  // [kSchedThreads]: keys of one round
+    // followed (nc <= kRankMax) by [npad] survivals q in rank order
     __shared__ unsigned long long s_base_local;
     __shared__ uint64_t s_base_part[kSchedMaxCluster];
     __shared__ uint64_t s_slot_v[kSchedMaxCluster];
@@ -234,22 +235,29 @@ __global__ void __launch_bounds__(kSchedThreads, 1) k_schedule(SchedArgs a) {
                 stage[tid] = c;
             }
             __syncthreads();
-            if (tid < ((nr + 31) & ~31)) {  // whole warps, for the sum below
-                uint64_t A = 0;
-                if (tid < nr) {
-                    const int b = r0 + tid;
-                    uint64_t* dst = split ? kst + tid * per : key + (size_t)b * per;
-                    double s = 1.0;
-                    A = surv_q(1.0);  // k = 0
-                    for (int k = 1; k <= G; ++k) {
-                        s = __dmul_rn(s, stage[tid * G + k - 1]);
-                        const uint64_t q = surv_q(s);
-                        if (k <= ml)
-                            A += q;
-                        else
-                            dst[k - ml - 1] = cand_key(q, k, b);
-                    }
+            // the products, one thread per request, each survival written back
+            // over its confidence (only the fp64 chain is sequential)
+            if (tid < nr) {
+                double* sr = stage + tid * G;
+                double s = 1.0;
+                for (int k = 0; k < G; ++k) {
+                    s = __dmul_rn(s, sr[k]);
+                    sr[k] = s;
                 }
+            }
+            __syncthreads();
+            // keys and the progress at min_len, one thread per (request, k)
+            {
+                uint64_t A = 0;
+                if (tid < nr * G) {
+                    const int j = tid / G, k = tid - j * G + 1, b = r0 + j;
+                    const uint64_t q = surv_q(stage[tid]);
+                    if (k <= ml)
+                        A = q;
+                    else
+                        (split ? kst + j * per : key + (size_t)b * per)[k - ml - 1] = cand_key(q, k, b);
+                }
+                if (tid < nr) A += surv_q(1.0);  // the k = 0 term of request r0 + tid
                 for (int o = 16; o > 0; o >>= 1) A += __shfl_xor_sync(0xffffffffu, A, o);
                 if (lane == 0 && A) atomicAdd(&s_base_local, (unsigned long long)A);
             }
@@ -279,34 +287,30 @@ __global__ void __launch_bounds__(kSchedThreads, 1) k_schedule(SchedArgs a) {
         base = s_base_local;
     }
 
-    // 2. sort the keys ascending (every CTA).  Each request's keys already
-    //    form an ascending run of `per`; up to kMergeMax candidates the runs
-    //    are merged pairwise, each key moving to its own index plus its
-    //    rank in the partner run; above that, a bitonic network.
-    if (nc <= kMergeMax) {
-        for (int L = per; L < nc; L <<= 1) {
-            uint64_t xv[kMergeMax / kSchedThreads];
-            int np[kMergeMax / kSchedThreads];
-#pragma unroll
-            for (int e = 0; e < kMergeMax / kSchedThreads; ++e) {
-                const int i = tid + e * kSchedThreads;
-                if (i < nc) {
-                    const uint64_t x = key[i];
-                    const int m = i / L, own = i - m * L;
-                    const int lo = (m ^ 1) * L, hi = min(nc, lo + L);
-                    const int cnt = lo < nc ? count_below(key + lo, hi - lo, x) : 0;
-                    xv[e] = x;
-                    np[e] = (m & ~1) * L + own + cnt;
-                }
+    if (!split) cluster_wait();  // every CTA of the cluster runs: stores across it follow
+
+    // 2. order the candidates.  Up to kRankMax candidates, by rank: each
+    //    request's keys already form an ascending run of `per`, so a key's rank
+    //    is the sum over runs of the keys below it; every CTA ranks its share
+    //    and stores (q, request) at that rank in every CTA.  Above that, a
+    //    bitonic network sorts the keys in every CTA.
+    uint64_t* qv = key;  // survivals q in candidate order after this step
+    if (nc <= kRankMax) {
+        uint64_t* sq = kst + kSchedThreads;  // [npad]
+        for (int i = nc + tid; i < npad; i += kSchedThreads) sq[i] = 0;
+        const int cpc = (nc + CL - 1) / CL, c_lo = min(nc, rank * cpc), c_hi = min(nc, c_lo + cpc);
+        for (int i = c_lo + warp; i < c_hi; i += kSchedThreads / 32) {
+            const uint64_t x = key[i];
+            int below = 0;
+            for (int r2 = lane; r2 < B; r2 += 32) below += count_below(key + r2 * per, per, x);
+            for (int o = 16; o > 0; o >>= 1) below += __shfl_xor_sync(0xffffffffu, below, o);
+            if (lane < CL) {
+                *cluster.map_shared_rank(&sq[below], lane) = kQField - (x >> 17);
+                *cluster.map_shared_rank(&cb[below], lane) = (uint16_t)(x & 4095u);
             }
-            __syncthreads();
-#pragma unroll
-            for (int e = 0; e < kMergeMax / kSchedThreads; ++e) {
-                const int i = tid + e * kSchedThreads;
-                if (i < nc) key[np[e]] = xv[e];
-            }
-            __syncthreads();
         }
+        cluster.sync();
+        qv = sq;
     } else {
         // bitonic: strides below 32 by warp shuffles, the others through
         // shared memory (npad >= 32, so the threads of a warp are all in or
@@ -334,18 +338,23 @@ __global__ void __launch_bounds__(kSchedThreads, 1) k_schedule(SchedArgs a) {
         }
     }
 
-    // 3. survivals q in sorted order, the request of each, and the count of
-    //    positive ones (a prefix, q being descending)
+    // 3. survivals q in sorted order (from the sorted keys on the bitonic
+    //    path), the request of each, and the count of positive ones (a prefix,
+    //    q being descending)
     int npos = 0;
     for (int i = tid; i < npad; i += kSchedThreads) {
-        const uint64_t kk = key[i];
-        uint64_t q = 0;
-        if (i < nc) {
-            q = kQField - (kk >> 17);
-            cb[i] = (uint16_t)(kk & 4095u);
+        if (qv == key) {
+            const uint64_t kk = key[i];
+            uint64_t q = 0;
+            if (i < nc) {
+                q = kQField - (kk >> 17);
+                cb[i] = (uint16_t)(kk & 4095u);
+            }
+            key[i] = q;
+            npos += q > 0;
+        } else {
+            npos += i < nc && qv[i] > 0;
         }
-        key[i] = q;
-        npos += q > 0;
     }
     for (int o = 16; o > 0; o >>= 1) npos += __shfl_xor_sync(0xffffffffu, npos, o);
     if (lane == 0 && npos) atomicAdd(&s_npos, npos);
@@ -358,7 +367,7 @@ __global__ void __launch_bounds__(kSchedThreads, 1) k_schedule(SchedArgs a) {
         const bool has = tid * E < npad;
         uint64_t run = 0;
         if (has)
-            for (int e = 0; e < E; ++e) run += key[tid * E + e];
+            for (int e = 0; e < E; ++e) run += qv[tid * E + e];
         uint64_t incl = run;
         for (int o = 1; o < 32; o <<= 1) {
             const uint64_t t = __shfl_up_sync(0xffffffffu, incl, o);
@@ -379,7 +388,7 @@ __global__ void __launch_bounds__(kSchedThreads, 1) k_schedule(SchedArgs a) {
         uint64_t off = base + s_red_v[warp] + (incl - run);
         if (has)
             for (int e = 0; e < E; ++e) {
-                off += key[tid * E + e];
+                off += qv[tid * E + e];
                 key[tid * E + e] = off;
             }
         __syncthreads();
@@ -423,7 +432,6 @@ __global__ void __launch_bounds__(kSchedThreads, 1) k_schedule(SchedArgs a) {
         const int take_best = __shfl_sync(0xffffffffu, take, bi & 31);
         if (lane == 0) s_dcut_k = take_best;
     }
-    if (!split) cluster_wait();  // every CTA of the cluster runs
     if (a.mode != SPEC_SCHED_DCUT) {
         if (a.mode == SPEC_SCHED_EXACT) {
             warp_best(bv, bi);
@@ -517,8 +525,11 @@ using namespace specv;
 
 namespace {
 
-// Dynamic shared memory of k_schedule for a padded candidate count.
-size_t sched_smem_bytes(int npad) { return (size_t)npad * 10 + (size_t)kSchedThreads * 16 + 16; }
+// Dynamic shared memory of k_schedule for a padded candidate count (the
+// ranked path keeps the survivals in rank order in a second array).
+size_t sched_smem_bytes(int npad, int nc) {
+    return (size_t)npad * 10 + (size_t)kSchedThreads * 16 + 16 + (nc <= kRankMax ? (size_t)npad * 8 : 0);
+}
 
 // Cluster size of k_schedule per device: 16 CTAs where the GPU can place such
 // a cluster at the largest shared-memory size, else the portable 8; 0 = not
@@ -529,7 +540,7 @@ int sched_cluster_size(int dev) {
     if (g_sched_cluster[dev]) return g_sched_cluster[dev];
     int npad_max = 32;
     while (npad_max < SPEC_MAX_SCHED_CANDIDATES) npad_max <<= 1;
-    const size_t smem_max = sched_smem_bytes(npad_max);
+    const size_t smem_max = sched_smem_bytes(npad_max, SPEC_MAX_SCHED_CANDIDATES);
     if (cudaFuncSetAttribute((const void*)k_schedule, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem_max) != cudaSuccess)
         return 0;
@@ -623,7 +634,7 @@ int spec_schedule(const float* confidence, int B, int gamma, const spec_cost_tab
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cl);
     cfg.blockDim = dim3(kSchedThreads);
-    cfg.dynamicSmemBytes = sched_smem_bytes(npad);
+    cfg.dynamicSmemBytes = sched_smem_bytes(npad, a.nc);
     cfg.stream = (cudaStream_t)stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
