@@ -396,6 +396,23 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     sv.profile_events(None, None)
     k1_ms = sum(a.elapsed_time(b) for a, b in pairs) / len(pairs)
+    k1_list = sorted(a.elapsed_time(b) for a, b in pairs)
+
+    # timed region 3: each call bracketed by its own event pair (at call
+    # boundaries, where nothing overlaps) for the latency distribution
+    n_lat = min(args.steps, 1000)
+    cpairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_lat)]
+    torch.cuda.synchronize(dev)
+    for a, b in cpairs:
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    lat = sorted(a.elapsed_time(b) * 1e3 for a, b in cpairs)
+    pct = lambda v, q: v[min(len(v) - 1, int(q * (len(v) - 1) + 0.5))]
+    latency = {"unit": "us", "calls": n_lat, "p10": pct(lat, 0.1), "p50": pct(lat, 0.5), "p90": pct(lat, 0.9),
+               "k1_p10": pct(k1_list, 0.1) * 1e3, "k1_p50": pct(k1_list, 0.5) * 1e3,
+               "k1_p90": pct(k1_list, 0.9) * 1e3}
     status = sv.read_status(ws)
     n = out_n.cpu().numpy()
 
@@ -499,6 +516,7 @@ def run_ours(args):
         "gpu_launches": sv.kernel_count(B, case.T) * args.steps,
         "clocks": clk.summary(),
         "device_status": status,
+        "latency": latency,
         "scheduled_step": scheduled_step,
         "schedule": sched,
         "scheduled_step_packed": packed_step,

@@ -211,3 +211,17 @@ def test_schedule_pack_verify_in_one_graph(sv):
     assert sv.read_status(ws) == 0 and sv.read_status(sws) == 0
     pad = H.gpu_verify(case)
     assert (ref_t == pad["tokens"]).all() and (ref_n == pad["accept_len"]).all()
+
+
+@pytest.mark.parametrize("name", ["tiny", "greedy"])
+def test_packed_no_drafts(sv, name):
+    """gamma = 0: one target row per request, a pure draw from p (or its argmax)."""
+    case = specsynth.make_verify_case(name, B=5, gamma=0, V=3000)
+    vl = np.zeros(case.B, np.int32)
+    r = oracle.pack_rows(vl, 0)
+    assert (r["K_target"], r["K_draft"]) == (case.B, 0)
+    tp, dp = _pack(case, vl, r["target_row"], r["draft_row"], r["K_target"], r["K_draft"], 0)
+    g = _run_packed(sv, case, vl, tp, dp, r["target_row"], r["draft_row"])
+    pad = H.gpu_verify(case)
+    assert g["device_status"] == 0
+    assert (g["tokens"] == pad["tokens"]).all() and (g["accept_len"] == 0).all()

@@ -118,6 +118,21 @@ def test_ragged_verify_lengths_including_zero():
     assert (g["accept_len"] <= case.verify_len).all()
 
 
+@pytest.mark.parametrize("dtype,V", [("bf16", 2_500_001), ("bf16", 4_300_003), ("f32", 1_500_001),
+                                     ("f32", 2_200_001)])
+def test_very_large_vocabularies(dtype, V):
+    """More than 1024 chunks per row (round sums of the draw leave shared
+    memory) and more than 2048 (chunk totals go to the workspace)."""
+    case = specsynth.make_verify_case("tiny", B=4, gamma=2, V=V, dtype=dtype, seed_logits=800 + V % 97,
+                                      seed_noise=801, seed_tokens=802, seed_uniforms=803)
+    g, o, P = _run(case)
+    _report(f"V={V} {dtype}", P)
+    assert g["device_status"] == 0
+    assert not P.mismatches, P.mismatches[:3]
+    assert P.max_p_err <= H.PROB_TOL and P.max_mass_err <= H.PROB_TOL
+    assert (o["accept_len"] < case.gamma).any()      # at least one residual draw
+
+
 def test_large_batch_small_vocab():
     case = specsynth.make_verify_case("tiny", B=4096, gamma=4, V=64)
     g, o, P = _run(case)
