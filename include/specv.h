@@ -288,6 +288,20 @@ int spec_verify_static(const void* target_logits, const void* draft_logits, spec
                        const float* uniforms, int32_t* out_tokens, int32_t* out_accept_len,
                        spec_stream_t stream);
 
+/*
+ * Self-test of the bounded waits.  The streaming kernel waits on mbarriers for
+ * its own bulk copies; every such wait gives up after 2 s of the GPU's global
+ * timer and the call then reports SPEC_ERR_TIMEOUT instead of hanging.  This
+ * call runs the same wait routine with a limit of limit_ns (1e3 .. 2e9):
+ *   status[0], elapsed_ns[0]: a wait on a barrier nothing completes; expect
+ *                             SPEC_ERR_TIMEOUT after about limit_ns;
+ *   status[1], elapsed_ns[1]: a wait on a completed phase; expect SPEC_OK at once.
+ * status [2] int32 and elapsed_ns [2] uint64 are device pointers.  One launch
+ * of one warp.
+ */
+int spec_selftest_wait(long long limit_ns, int32_t* status, unsigned long long* elapsed_ns,
+                       spec_stream_t stream);
+
 /* ------------------------------------------------------------------ status */
 
 /* Synchronises `stream`, reads the sticky device status word of `workspace`

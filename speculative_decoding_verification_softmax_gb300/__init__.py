@@ -35,7 +35,7 @@ EXPORTED = ["spec_verify_workspace_bytes", "spec_verify", "spec_verify_stats",
             "spec_schedule_workspace_bytes", "spec_schedule", "spec_read_status",
             "spec_status_string", "spec_profile_events", "spec_verify_kernel_count",
             "spec_verify_static", "spec_schedule_static", "spec_sts_fit", "spec_verify_packed",
-            "spec_pack_rows"]
+            "spec_pack_rows", "spec_selftest_wait"]
 STATIC_WORKSPACE_BYTES = 8 << 20
 
 
@@ -127,6 +127,8 @@ def lib():
                 L.spec_verify_packed.restype = i32
                 L.spec_pack_rows.argtypes = [vp, i32, i32, vp, vp, vp, vp]
                 L.spec_pack_rows.restype = i32
+                L.spec_selftest_wait.argtypes = [ctypes.c_longlong, vp, vp, vp]
+                L.spec_selftest_wait.restype = i32
                 _lib = L
     return _lib
 
@@ -391,6 +393,17 @@ def sts_fit(confidence, accept_len):
                             T.ctypes.data_as(ctypes.c_void_p), e.ctypes.data_as(ctypes.c_void_p))
     _check(rc, "spec_sts_fit")
     return T, e
+
+
+def selftest_wait(limit_ns: int = 1_000_000, stream=None):
+    """Run spec_selftest_wait: returns ((status_blocked, status_completed),
+    (elapsed_ns_blocked, elapsed_ns_completed)) after synchronising."""
+    torch = _torch()
+    st = torch.full((2,), 99, dtype=torch.int32, device="cuda")
+    el = torch.zeros((2,), dtype=torch.int64, device="cuda")
+    _check(lib().spec_selftest_wait(int(limit_ns), _ptr(st), _ptr(el), _stream_handle(stream)), "spec_selftest_wait")
+    torch.cuda.synchronize()
+    return tuple(int(v) for v in st.cpu()), tuple(int(v) for v in el.cpu())
 
 
 def read_status(workspace, stream=None) -> int:

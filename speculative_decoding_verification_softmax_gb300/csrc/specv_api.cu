@@ -21,6 +21,38 @@ int spec_read_status(void* workspace, spec_stream_t stream, int* status) {
     return SPEC_OK;
 }
 
+namespace {
+
+// Self-test of the bounded mbarrier wait that the streaming kernel relies on:
+// slot 0 waits on a barrier that nothing completes (the wait must give up
+// after limit_ns and report SPEC_ERR_TIMEOUT), slot 1 on one whose phase has
+// completed (the wait must succeed at once).
+__global__ void k_wait_selftest(unsigned long long limit_ns, int32_t* status, unsigned long long* elapsed_ns) {
+    __shared__ __align__(8) uint64_t bars[2];
+    if (threadIdx.x != 0) return;
+    specv::mbar_init(&bars[0], 1);
+    specv::mbar_init(&bars[1], 1);
+    specv::fence_mbar_init();
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(specv::smem_u32(&bars[1])) : "memory");
+    for (int i = 0; i < 2; ++i) {
+        const unsigned long long t0 = specv::globaltimer_ns();
+        const bool done = specv::mbar_wait_bounded(&bars[i], 0, limit_ns);
+        elapsed_ns[i] = specv::globaltimer_ns() - t0;
+        status[i] = done ? SPEC_OK : SPEC_ERR_TIMEOUT;
+    }
+}
+
+}  // namespace
+
+extern "C" int spec_selftest_wait(long long limit_ns, int32_t* status, unsigned long long* elapsed_ns,
+                                  spec_stream_t stream) {
+    if (limit_ns < 1000 || limit_ns > 2000000000ll) return SPEC_ERR_SHAPE;
+    if (!status || !elapsed_ns) return SPEC_ERR_NULL;
+    if (((uintptr_t)status & 3) || ((uintptr_t)elapsed_ns & 7)) return SPEC_ERR_ALIGN;
+    k_wait_selftest<<<1, 32, 0, (cudaStream_t)stream>>>((unsigned long long)limit_ns, status, elapsed_ns);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
 // Sequential Temperature Scaling fit on the host ("UraionSpec" §2.4, §3.6).
 int spec_sts_fit(const float* confidence, const int32_t* accept_len, int n, int gamma, float* out_temperature,
                  double* out_ece) {

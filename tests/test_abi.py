@@ -153,6 +153,13 @@ def test_pack_rows_host_errors(L):
     assert L.spec_pack_rows(FAKE, 4, 4, ctypes.c_void_p(0x10001), FAKE, FAKE, None) == sv.ERR_ALIGN
 
 
+def test_selftest_wait_host_errors(L):
+    assert L.spec_selftest_wait(10, FAKE, FAKE, None) == sv.ERR_SHAPE
+    assert L.spec_selftest_wait(10 ** 10, FAKE, FAKE, None) == sv.ERR_SHAPE
+    assert L.spec_selftest_wait(10 ** 6, None, FAKE, None) == sv.ERR_NULL
+    assert L.spec_selftest_wait(10 ** 6, FAKE, ctypes.c_void_p(0x10004), None) == sv.ERR_ALIGN
+
+
 def test_status_strings(L):
     for code in range(-14, 1):
         assert sv.status_string(code) and "unknown" not in sv.status_string(code)
