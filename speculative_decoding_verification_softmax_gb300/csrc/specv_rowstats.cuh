@@ -59,11 +59,11 @@ struct StatsArgs {
 // Rows a request needs: target 0..ell and (T > 0) draft 0..ell-1; 0 when
 // verify_len is out of range or packed rows fall outside the packed arrays
 // (the finish kernel marks the request invalid).
-template <bool GREEDY>
+template <bool GREEDY, bool PACKED>
 __device__ __forceinline__ int rows_of(const int32_t* verify_len, const RowMap& rm, int b, int gamma) {
     const int ell = verify_len ? verify_len[b] : gamma;
     if (ell < 0 || ell > gamma) return 0;
-    if (!rows_in_range(rm, b, ell, !GREEDY)) return 0;
+    if (PACKED && !rows_in_range(rm, b, ell, !GREEDY)) return 0;
     return GREEDY ? ell + 1 : 2 * ell + 1;
 }
 
@@ -76,7 +76,7 @@ __device__ __forceinline__ int row_id(int b, int k, int cnt, int gamma, int T1) 
 
 // prefix[b] = rows of requests < b, prefix[B] = total.  Whole CTA; ends
 // with a barrier, so every thread sees the prefix.
-template <bool GREEDY>
+template <bool GREEDY, bool PACKED>
 __device__ void block_row_prefix(const int32_t* verify_len, const RowMap& rm, int B, int gamma, int* prefix) {
     __shared__ int s_w[32];
     __shared__ int s_total;
@@ -87,7 +87,7 @@ __device__ void block_row_prefix(const int32_t* verify_len, const RowMap& rm, in
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
         const int b = tid * PER + i;
-        cnt[i] = b < B ? rows_of<GREEDY>(verify_len, rm, b, gamma) : 0;
+        cnt[i] = b < B ? rows_of<GREEDY, PACKED>(verify_len, rm, b, gamma) : 0;
         mine += cnt[i];
     }
     int incl = mine;
@@ -266,7 +266,9 @@ __device__ __forceinline__ float2 chunk_stats(const uint4* sm, int nvec_rt, int 
     return make_float2(Mc, warp_sum((a0 + a1) + (a2 + a3)));
 }
 
-template <int ES, bool GREEDY, bool ALIGNED>
+// PACKED: rows addressed through the row index of a packed layout (the
+// padded layout's kernels carry none of that code).
+template <int ES, bool GREEDY, bool ALIGNED, bool PACKED>
 __global__ void __launch_bounds__(kStatsThreads, 1) k_row_stats(StatsArgs a, Layout L) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 127) & ~uintptr_t(127));
@@ -287,7 +289,7 @@ __global__ void __launch_bounds__(kStatsThreads, 1) k_row_stats(StatsArgs a, Lay
         for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
         fence_mbar_init();
     }
-    block_row_prefix<GREEDY>(a.verify_len, a.rm, a.B, a.gamma, prefix);
+    block_row_prefix<GREEDY, PACKED>(a.verify_len, a.rm, a.B, a.gamma, prefix);
     pdl_trigger();
 
     const int nch = L.nch;
@@ -301,7 +303,9 @@ __global__ void __launch_bounds__(kStatsThreads, 1) k_row_stats(StatsArgs a, Lay
     const long long count = has_items ? (total - gw + W - 1) / W : 0;  // items of this warp
     const int Wq = W / nch, Wr = W - Wq * nch;
     const int T1 = a.B * (a.gamma + 1);
-    const bool use_table = n_rows <= kTableRows;
+    // the row table pays off only when warps take more items than the first
+    // kStages (issued from the prefix before the table could exist)
+    const bool use_table = n_rows <= kTableRows && total > (long long)W * kStages;
     bool table_ready = false;  // the first copies are issued before the table is built
 
     // A cursor over this warp's items: (compact row, chunk) and the request
@@ -324,7 +328,7 @@ __global__ void __launch_bounds__(kStatsThreads, 1) k_row_stats(StatsArgs a, Lay
         return row_id<GREEDY>(k.b, k.r - prefix[k.b], cnt, a.gamma, T1);
     };
     auto row_ptr = [&](int g) -> const char* {
-        if (!a.rm.trow) return g < T1 ? a.target + (size_t)g * a.V * ES : a.draft + (size_t)(g - T1) * a.V * ES;
+        if constexpr (!PACKED) return g < T1 ? a.target + (size_t)g * a.V * ES : a.draft + (size_t)(g - T1) * a.V * ES;
         if (g < T1) {
             const int b = g / (a.gamma + 1);
             return a.target + target_row(a.rm, b, g - b * (a.gamma + 1), a.gamma + 1) * a.V * ES;

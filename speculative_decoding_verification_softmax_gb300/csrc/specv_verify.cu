@@ -472,13 +472,28 @@ constexpr int kChunkSmem = 2048;  // chunk totals kept in rank 0's shared memory
 constexpr int kRoundSmem = 1024;  // chunks whose round sums are kept there too
 
 // CTAs per request: enough warps for the rows to merge and the chunks to sum.
-inline int finish_cluster_size(int gamma, int nch, bool greedy) {
+inline int finish_cluster_size(int B, int gamma, int nch, bool greedy, int sms) {
     const int rows = greedy ? gamma + 1 : 2 * gamma + 1;
     const int work = greedy ? rows : std::max(rows, nch);
-    return std::min(kMaxCluster, std::max(1, (work + kFinWarps - 1) / kFinWarps));
+    const int by_work = (work + kFinWarps - 1) / kFinWarps;
+    // small batches at T > 0: spread each request's residual sums over more SMs
+    const int by_fill = greedy ? 1 : (2 * sms + B - 1) / B;
+    return std::min(kMaxCluster, std::max(1, std::max(by_work, by_fill)));
 }
 
-template <int ES, bool GREEDY>
+// Parts per full-vector chunk in the residual sums: a chunk's 8 rounds are
+// split over f warps (8 / f rounds each, one memory round trip) when the
+// cluster has at least 2 f warps per chunk.  The same value in both phases.
+__host__ __device__ inline int residual_split(int nch, int nw) {
+    int f = 1;
+    while (f < 8 && nch * f * 2 <= nw) f *= 2;
+    return f;
+}
+
+// SPLIT: the residual sums are split into (chunk, round group) tasks (small
+// vocabularies with warps to spare); a separate instantiation, so that the
+// common path's register allocation does not carry that code.
+template <int ES, bool GREEDY, bool SPLIT>
 __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout L) {
     cg::cluster_group cluster = cg::this_cluster();
     const int cs = (int)cluster.num_blocks();
@@ -639,7 +654,45 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
     float* rchunk = (float*)(a.ws + L.rchunk) + (size_t)b * L.nch;
     const bool tot_smem = L.nch <= kChunkSmem;
     const bool round_smem = L.nch <= kRoundSmem;
-    if (job.mode == 1) {
+    const int fsplit = SPLIT && round_smem ? residual_split(L.nch, nw) : 1;
+    if (SPLIT && job.mode == 1 && fsplit > 1) {
+        // (chunk, round group) tasks; chunk totals are summed from the round
+        // sums by rank 0 before the draw
+        const int R = 8 / fsplit;
+        for (int task = gw; task < L.nch * fsplit; task += nw) {
+            const int c = task / fsplit, part = task - c * fsplit;
+            const int e0 = c * L.CH, e1 = min(a.V, e0 + L.CH);
+            if (chunk_vec<ES>(job, rt, rd, e0, e1)) {
+                const int nvec = (e1 - e0) * ES / 16;
+                const uint4* vt = (const uint4*)(rt + (size_t)e0 * ES);
+                const uint4* vd = (const uint4*)(rd + (size_t)e0 * ES);
+                uint4 tv[4], dv[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int i = 32 * (part * R + k) + lane;
+                    tv[k] = dv[k] = make_uint4(0, 0, 0, 0);
+                    if (k < R && i < nvec) {
+                        tv[k] = __ldg(vt + i);
+                        dv[k] = __ldg(vd + i);
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    if (k < R) {
+                        const int i = 32 * (part * R + k) + lane;
+                        const float w = i < nvec ? vec_weight_sum_ordered<ES>(job, tv[k], dv[k], a.c_hi, a.c_lo) : 0.f;
+                        const float rsum = warp_sum(w);
+                        if (lane == 0) *cluster.map_shared_rank(&s_rsum[c][part * R + k], 0) = rsum;
+                    }
+                }
+            } else if (part == 0) {
+                int lpos;
+                const float ls = seg_weight_sum<ES>(job, rt, rd, e0, e1, false, lane, a.c_hi, a.c_lo, lpos);
+                const DF tot = warp_sum_df(DF{ls, 0.f});
+                if (lane == 0) *cluster.map_shared_rank(&s_ctot[c], 0) = tot.hi + tot.lo;
+            }
+        }
+    } else if (!SPLIT && job.mode == 1) {
         for (int c = gw; c < L.nch; c += nw) {
             const int e0 = c * L.CH, e1 = min(a.V, e0 + L.CH);
             float t;
@@ -669,6 +722,19 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
     if (rank != 0 || warp != 0) return;
 
     // 5. the draw (rank 0, warp 0)
+    if (SPLIT && job.mode == 1 && fsplit > 1) {
+        // totals of the split chunks from their round sums, in round order
+        for (int c = lane; c < L.nch; c += 32) {
+            const int e0 = c * L.CH, e1 = min(a.V, e0 + L.CH);
+            if (chunk_vec<ES>(job, rt, rd, e0, e1)) {
+                DF acc = {0.f, 0.f};
+#pragma unroll
+                for (int k = 0; k < 8; ++k) acc = df_add(acc, DF{s_rsum[c][k], 0.f});
+                s_ctot[c] = acc.hi + acc.lo;
+            }
+        }
+        __syncwarp();
+    }
     const float2* tpart = partial + (size_t)job.g_t * L.nch;
     auto total_of = [&](const ReqState& js, int c) -> float {
         if (js.mode == 1) return tot_smem ? s_ctot[c] : __ldcg(rchunk + c);
@@ -841,11 +907,15 @@ int device_info(int& sms) {
     if (!d.attrs_set) {
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return SPEC_ERR_CUDA;
-        const void* fns[8] = {
-            (const void*)k_row_stats<2, false, false>, (const void*)k_row_stats<2, true, false>,
-            (const void*)k_row_stats<4, false, false>, (const void*)k_row_stats<4, true, false>,
-            (const void*)k_row_stats<2, false, true>,  (const void*)k_row_stats<2, true, true>,
-            (const void*)k_row_stats<4, false, true>,  (const void*)k_row_stats<4, true, true>};
+        const void* fns[16] = {
+            (const void*)k_row_stats<2, false, false, false>, (const void*)k_row_stats<2, true, false, false>,
+            (const void*)k_row_stats<4, false, false, false>, (const void*)k_row_stats<4, true, false, false>,
+            (const void*)k_row_stats<2, false, true, false>,  (const void*)k_row_stats<2, true, true, false>,
+            (const void*)k_row_stats<4, false, true, false>,  (const void*)k_row_stats<4, true, true, false>,
+            (const void*)k_row_stats<2, false, false, true>,  (const void*)k_row_stats<2, true, false, true>,
+            (const void*)k_row_stats<4, false, false, true>,  (const void*)k_row_stats<4, true, false, true>,
+            (const void*)k_row_stats<2, false, true, true>,   (const void*)k_row_stats<2, true, true, true>,
+            (const void*)k_row_stats<4, false, true, true>,   (const void*)k_row_stats<4, true, true, true>};
         for (const void* f : fns)
             if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStatsSmem) !=
                 cudaSuccess)
@@ -869,15 +939,20 @@ int launch_chain(const StatsArgs& sa, const FinishArgs& fa, const Layout& L, int
                  cudaStream_t st) {
     const long long max_items = (long long)L.R * L.nch;
     const int grid = (int)std::min<long long>(sms, (max_items + kStatsWarps - 1) / kStatsWarps);
+    const bool packed = sa.rm.trow != nullptr;
     if (g_ev_before) cudaEventRecord(g_ev_before, st);
-    if (aligned_rows)
-        k_row_stats<ES, GREEDY, true><<<grid, kStatsThreads, kStatsSmem, st>>>(sa, L);
-    else
-        k_row_stats<ES, GREEDY, false><<<grid, kStatsThreads, kStatsSmem, st>>>(sa, L);
+    if (aligned_rows) {
+        if (packed) k_row_stats<ES, GREEDY, true, true><<<grid, kStatsThreads, kStatsSmem, st>>>(sa, L);
+        else k_row_stats<ES, GREEDY, true, false><<<grid, kStatsThreads, kStatsSmem, st>>>(sa, L);
+    } else {
+        if (packed) k_row_stats<ES, GREEDY, false, true><<<grid, kStatsThreads, kStatsSmem, st>>>(sa, L);
+        else k_row_stats<ES, GREEDY, false, false><<<grid, kStatsThreads, kStatsSmem, st>>>(sa, L);
+    }
     if (g_ev_after) cudaEventRecord(g_ev_after, st);
     // one cluster per request; it may be scheduled while the streaming kernel
     // finishes and waits for its results with griddepcontrol.wait
-    const int cs = finish_cluster_size(sa.gamma, L.nch, GREEDY);
+    const int cs = finish_cluster_size(sa.B, sa.gamma, L.nch, GREEDY, sms);
+    const bool split = !GREEDY && L.nch <= kRoundSmem && residual_split(L.nch, cs * kFinWarps) > 1;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -892,7 +967,10 @@ int launch_chain(const StatsArgs& sa, const FinishArgs& fa, const Layout& L, int
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    if (cudaLaunchKernelEx(&cfg, k_finish<ES, GREEDY>, fa, L) != cudaSuccess) return SPEC_ERR_CUDA;
+    cudaError_t e;
+    if (GREEDY || !split) e = cudaLaunchKernelEx(&cfg, k_finish<ES, GREEDY, false>, fa, L);
+    else e = cudaLaunchKernelEx(&cfg, k_finish<ES, GREEDY, !GREEDY>, fa, L);
+    if (e != cudaSuccess) return SPEC_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
