@@ -271,6 +271,63 @@ def time_schedulers(sv, dev, stream, rank: int):
             "kernel_launches_per_call": 1, "modes": res}
 
 
+def time_other_workloads(sv, specsynth, dev, stream, rank: int):
+    """Device time per call of the other verification workloads (the small
+    ones are latency-bound): 100 calls captured in a CUDA graph and replayed,
+    inputs rotated over copies so that each call's working set exceeds twice
+    the L2 where that takes at most 32 copies."""
+    import torch
+    from tests import _helpers as H
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    out = {}
+    for name in ("tiny", "mtp_chat", "greedy"):
+        case = specsynth.make_verify_case(name)
+        B, gamma, V = case.B, case.gamma, case.V
+        bytes_call = case.target.nbytes + (case.draft.nbytes if case.T != 0 else 0)
+        n_sets = max(1, min(32, -(-2 * l2 // bytes_call)))
+        sets = [H.to_device(case, dev) for _ in range(n_sets)]
+        dt = sv.BF16 if case.dtype == "bf16" else sv.F32
+        ws = sv.alloc_verify_workspace(B, gamma, V, dt, dev)
+        ot = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
+        on = torch.empty((B,), dtype=torch.int32, device=dev)
+
+        def call(i):
+            t, d, x, vl, u = sets[i % n_sets]
+            sv.verify(t, d, x, vl, case.T, u if case.T != 0 else None, out_tokens=ot, out_accept_len=on,
+                      workspace=ws)
+
+        for i in range(3):
+            call(i)
+        torch.cuda.synchronize(dev)
+        n_calls = 100
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                for i in range(n_calls):
+                    call(i)
+        stream.wait_stream(side)
+        g.replay()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(side):
+            e0.record(side)
+            for _ in range(5):
+                g.replay()
+            e1.record(side)
+        torch.cuda.synchronize(dev)
+        us = e0.elapsed_time(e1) * 1e3 / (5 * n_calls)
+        if sv.read_status(ws) != 0:
+            raise RuntimeError(f"device status on {name}")
+        out[name] = {"shape": f"B={B}, gamma={gamma}, V={V}, {case.dtype}, T={case.T:g}",
+                     "us_per_call": us, "verified_rows_per_s": B * gamma / (us / 1e6),
+                     "logit_bytes_per_call": bytes_call, "input_copies": n_sets,
+                     "l2_note": "working set > 2x L2" if n_sets * bytes_call > 2 * l2 else "L2-resident"}
+        del sets
+    return {"timing": "100 calls in a CUDA graph, 5 replays, CUDA events", "workloads": out}
+
+
 def time_packed_step(sv, specsynth, case, t, d, x, u, dev, stream, rank: int, steps: int):
     """D-cut budget, dense packing and verification on packed logits: the
     deployed path of the scheduled workload.  The ratio costs C(B, rho) are the
@@ -448,6 +505,7 @@ def run_ours(args):
                       "kernel_launches_per_step": 1 + sv.kernel_count(B, case.T)}
     sched = time_schedulers(sv, dev, stream, rank)
     packed_step = time_packed_step(sv, specsynth, case, t, d, x, u, dev, stream, rank, s_steps)
+    others = time_other_workloads(sv, specsynth, dev, stream, rank)
 
     # end to end through the public API: pinned host inputs -> device -> verify -> host outputs
     h_t = torch.from_numpy(case.target.view(np.int16)).pin_memory()
@@ -520,6 +578,7 @@ def run_ours(args):
         "scheduled_step": scheduled_step,
         "schedule": sched,
         "scheduled_step_packed": packed_step,
+        "other_workloads": others,
         "mean_accept_len": float(n.mean()),
     }
     print(json.dumps(line), flush=True)
