@@ -33,8 +33,7 @@ struct ReqState {
     float M_t;   // integer row scale of the target draw row
     float M_d;   // integer row scale of the draft draw row
     float rho_hi, rho_lo;  // S_t / S_d as an unevaluated float pair
-    int pad;
-    double S_t;  // row sum of the target draw row
+    float S_hi, S_lo;      // row sum of the target draw row, unevaluated float pair
 };
 
 // Unevaluated sum hi + lo of two floats (about 48 significant bits).
@@ -113,8 +112,8 @@ struct Layout {
         hdr = o;      o = up(o + 256);
         partial = o;  o = up(o + sizeof(float2) * (size_t)R * (size_t)nch);
         req = o;      o = up(o + sizeof(ReqState) * (size_t)B);
-        pq = o;       o = up(o + 2 * sizeof(double) * (size_t)B * (size_t)(gamma > 0 ? gamma : 1));
-        mass = o;     o = up(o + sizeof(double) * (size_t)B);
+        pq = o;       o = up(o + 2 * sizeof(float) * (size_t)B * (size_t)(gamma > 0 ? gamma : 1));
+        mass = o;     o = up(o + sizeof(float2) * (size_t)B);
         rchunk = o;   o = up(o + sizeof(float) * (size_t)B * (size_t)nch);
         total = o;
     }

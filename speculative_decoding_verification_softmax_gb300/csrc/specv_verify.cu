@@ -566,7 +566,8 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
             if (__any_sync(0xffffffffu, bad)) st = SPEC_ERR_NONFINITE;
         }
         int32_t* ot = a.out_tokens + (size_t)b * G1;
-        double* pq = (double*)(a.ws + L.pq);
+        float2* pq = (float2*)(a.ws + L.pq);  // p(x), q(x) diagnostics (fp32; widened by k_copy_stats)
+        float2* mass = (float2*)(a.ws + L.mass);
         ReqState o;
         o.ell = ell;
         o.status = st;
@@ -574,18 +575,15 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
         o.mode = 0;
         o.g_t = o.g_d = -1;
         o.u = o.M_t = o.M_d = o.rho_hi = o.rho_lo = 0.f;
-        o.pad = 0;
-        o.S_t = 0.0;
+        o.S_hi = o.S_lo = 0.f;
         if (st != SPEC_OK) {
             if (rank == 0) {
                 for (int k = lane; k <= a.gamma; k += 32) ot[k] = -1;
-                for (int k = lane; k < a.gamma; k += 32) {
-                    pq[2 * ((size_t)b * a.gamma + k)] = __longlong_as_double(0x7ff8000000000000ll);
-                    pq[2 * ((size_t)b * a.gamma + k) + 1] = __longlong_as_double(0x7ff8000000000000ll);
-                }
+                for (int k = lane; k < a.gamma; k += 32)
+                    pq[(size_t)b * a.gamma + k] = make_float2(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000));
                 if (lane == 0) {
                     a.out_accept_len[b] = -1;
-                    ((double*)(a.ws + L.mass))[b] = __longlong_as_double(0x7ff8000000000000ll);
+                    mass[b] = make_float2(__int_as_float(0x7fc00000), 0.f);
                     set_status(&hdr[kHdrStatus], st);
                 }
             }
@@ -609,7 +607,8 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
             o.n = n;
             o.g_t = b * G1 + n;
             o.M_t = s_row[n].M;
-            o.S_t = df_to_d(St);
+            o.S_hi = St.hi;
+            o.S_lo = St.lo;
             if (!GREEDY && n < ell) {
                 o.mode = 1;
                 o.g_d = T1 + b * a.gamma + n;
@@ -623,17 +622,14 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
                 o.u = ub;
             }
             if (rank == 0) {
-                if (j < a.gamma) {
-                    pq[2 * ((size_t)b * a.gamma + j)] = (double)px;
-                    pq[2 * ((size_t)b * a.gamma + j) + 1] = (double)qx;
-                }
+                if (j < a.gamma) pq[(size_t)b * a.gamma + j] = make_float2(px, qx);
                 // lane k holds draft token k; slot gamma (32 at most) needs lane 0's help
                 if (lane < n) ot[lane] = x;
                 else if (lane > n && lane <= a.gamma) ot[lane] = -1;
                 if (lane == 0 && a.gamma == 32 && n < 32) ot[32] = -1;
                 if (lane == 0) {
                     a.out_accept_len[b] = n;
-                    ((double*)(a.ws + L.mass))[b] = __longlong_as_double(0x7ff8000000000000ll);
+                    mass[b] = make_float2(__int_as_float(0x7fc00000), 0.f);
                     if (GREEDY) ot[n] = s_row[n].arg;
                 }
             }
@@ -796,7 +792,7 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
     }
     if (lane == 0) {
         a.out_tokens[(size_t)b * G1 + job.n] = tok;
-        ((double*)(a.ws + L.mass))[b] = df_to_d(W) / job.S_t;
+        ((float2*)(a.ws + L.mass))[b] = make_float2(W.hi, W.lo);  // divided by S_t in k_copy_stats
     }
 }
 
@@ -804,15 +800,19 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
 __global__ void k_copy_stats(const char* ws, Layout L, int B, int gamma, double* px, double* qx,
                              double* mass, int32_t* status) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    const double* pq = (const double*)(ws + L.pq);
+    const float2* pq = (const float2*)(ws + L.pq);
     if (i < B * gamma) {
-        if (px) px[i] = pq[2 * (size_t)i];
-        if (qx) qx[i] = pq[2 * (size_t)i + 1];
+        if (px) px[i] = (double)pq[i].x;
+        if (qx) qx[i] = (double)pq[i].y;
     }
     if (i < B) {
         const ReqState rs = ((const ReqState*)(ws + L.req))[i];
-        if (mass) mass[i] = rs.status == SPEC_OK ? ((const double*)(ws + L.mass))[i]
-                                                 : __longlong_as_double(0x7ff8000000000000ll);
+        const float2 w = ((const float2*)(ws + L.mass))[i];
+        // the draw's total weight over the target row sum, both float pairs
+        if (mass)
+            mass[i] = rs.status == SPEC_OK
+                          ? ((double)w.x + (double)w.y) / ((double)rs.S_hi + (double)rs.S_lo)
+                          : __longlong_as_double(0x7ff8000000000000ll);
         if (status) status[i] = rs.status;
     }
 }
