@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(kSchedThreads, 1) k_schedule(SchedArgs a) {
     uint16_t* cb = (uint16_t*)(key + a.npad);            // [npad]: request of each sorted candidate
     double* stage = (double*)(cb + a.npad);              // [kSchedThreads]: confidences of one round
     uint64_t* kst = (uint64_t*)(stage + kSchedThreads);  // [kSchedThreads]: keys of one round
-    // followed (nc <= kRankMax) by [npad] survivals q in rank order
+    // followed (nc <= kRankMax) by [npad] keys in rank order
     __shared__ unsigned long long s_base_local;
     __shared__ uint64_t s_base_part[kSchedMaxCluster];
     __shared__ uint64_t s_slot_v[kSchedMaxCluster];
@@ -292,9 +292,10 @@ __global__ void __launch_bounds__(kSchedThreads, 1) k_schedule(SchedArgs a) {
     // 2. order the candidates.  Up to kRankMax candidates, by rank: each
     //    request's keys already form an ascending run of `per`, so a key's rank
     //    is the sum over runs of the keys below it; every CTA ranks its share
-    //    and stores (q, request) at that rank in every CTA.  Above that, a
-    //    bitonic network sorts the keys in every CTA.
-    uint64_t* qv = key;  // survivals q in candidate order after this step
+    //    and stores the key at that rank in every CTA (one 64-bit store per
+    //    CTA and candidate).  Above that, a bitonic network sorts the keys in
+    //    every CTA.
+    uint64_t* qv = key;  // keys in candidate order after this step, then their survivals q
     if (nc <= kRankMax) {
         uint64_t* sq = kst + kSchedThreads;  // [npad]
         for (int i = nc + tid; i < npad; i += kSchedThreads) sq[i] = 0;
@@ -304,10 +305,7 @@ __global__ void __launch_bounds__(kSchedThreads, 1) k_schedule(SchedArgs a) {
             int below = 0;
             for (int r2 = lane; r2 < B; r2 += 32) below += count_below(key + r2 * per, per, x);
             for (int o = 16; o > 0; o >>= 1) below += __shfl_xor_sync(0xffffffffu, below, o);
-            if (lane < CL) {
-                *cluster.map_shared_rank(&sq[below], lane) = kQField - (x >> 17);
-                *cluster.map_shared_rank(&cb[below], lane) = (uint16_t)(x & 4095u);
-            }
+            if (lane < CL) *cluster.map_shared_rank(&sq[below], lane) = x;
         }
         cluster.sync();
         qv = sq;
@@ -338,23 +336,18 @@ __global__ void __launch_bounds__(kSchedThreads, 1) k_schedule(SchedArgs a) {
         }
     }
 
-    // 3. survivals q in sorted order (from the sorted keys on the bitonic
-    //    path), the request of each, and the count of positive ones (a prefix,
-    //    q being descending)
+    // 3. survivals q in sorted order from the sorted keys, the request of
+    //    each, and the count of positive ones (a prefix, q being descending)
     int npos = 0;
     for (int i = tid; i < npad; i += kSchedThreads) {
-        if (qv == key) {
-            const uint64_t kk = key[i];
-            uint64_t q = 0;
-            if (i < nc) {
-                q = kQField - (kk >> 17);
-                cb[i] = (uint16_t)(kk & 4095u);
-            }
-            key[i] = q;
-            npos += q > 0;
-        } else {
-            npos += i < nc && qv[i] > 0;
+        const uint64_t kk = qv[i];
+        uint64_t q = 0;
+        if (i < nc) {
+            q = kQField - (kk >> 17);
+            cb[i] = (uint16_t)(kk & 4095u);
         }
+        qv[i] = q;
+        npos += q > 0;
     }
     for (int o = 16; o > 0; o >>= 1) npos += __shfl_xor_sync(0xffffffffu, npos, o);
     if (lane == 0 && npos) atomicAdd(&s_npos, npos);
