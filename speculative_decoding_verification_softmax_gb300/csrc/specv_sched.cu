@@ -196,6 +196,15 @@ __global__ void __launch_bounds__(kSchedThreads, 1) k_schedule(SchedArgs a) {
     if (!split) cluster_arrive_relaxed();  // waited on before the first store to another CTA
     __syncthreads();
 
+    // the objective slice of this CTA: budgets K in [k_lo, k_lo + ccnt)
+    // (exact scan and Algorithm 1); their round costs, one per thread while
+    // the survival chains run, in csl[0 .. ccnt] (one past the slice for
+    // Algorithm 1's look-ahead)
+    const double N0 = __dmul_rn((double)B, (double)(ml + 1));
+    const int cpc = (nc + 1 + CL - 1) / CL;
+    const int k_lo = min(nc + 1, rank * cpc), ccnt = min(nc + 1, k_lo + cpc) - k_lo;
+    double* csl = (double*)(kst + kSchedThreads + (nc <= kRankMax ? npad : 0));
+    bool costs_done = a.mode == SPEC_SCHED_DCUT;
     uint64_t base = 0;
     if (split) {
         // every CTA checks the whole input, so that all take the same branch
@@ -219,6 +228,7 @@ __global__ void __launch_bounds__(kSchedThreads, 1) k_schedule(SchedArgs a) {
         const int bpc = split ? (B + CL - 1) / CL : B;
         const int b_lo = min(B, rank * (split ? bpc : 0)), b_hi = min(B, b_lo + bpc);
         const int R = kSchedThreads / max(G, 1);
+        costs_done = false;
         for (int r0 = b_lo; r0 < b_hi; r0 += R) {
             const int nr = min(R, b_hi - r0);
             if (tid < nr * G) {
@@ -244,7 +254,13 @@ __global__ void __launch_bounds__(kSchedThreads, 1) k_schedule(SchedArgs a) {
                     s = __dmul_rn(s, sr[k]);
                     sr[k] = s;
                 }
+            } else if (!costs_done) {
+                // meanwhile the idle threads take the round costs C(N0 + K)
+                // of this CTA's objective slice (they do not depend on the order)
+                for (int j = tid - nr; j <= ccnt; j += kSchedThreads - nr)
+                    csl[j] = cost_at(__dadd_rn(N0, (double)(k_lo + j)), a);
             }
+            costs_done = costs_done || nr < kSchedThreads;
             __syncthreads();
             // keys and the progress at min_len, one thread per (request, k)
             {
@@ -287,6 +303,10 @@ __global__ void __launch_bounds__(kSchedThreads, 1) k_schedule(SchedArgs a) {
         base = s_base_local;
     }
 
+    if (!costs_done) {
+        for (int j = tid; j <= ccnt; j += kSchedThreads) csl[j] = cost_at(__dadd_rn(N0, (double)(k_lo + j)), a);
+        __syncthreads();
+    }
     if (!split) cluster_wait();  // every CTA of the cluster runs: stores across it follow
 
     // 2. order the candidates.  Up to kRankMax candidates, by rank: each
@@ -387,15 +407,13 @@ __global__ void __launch_bounds__(kSchedThreads, 1) k_schedule(SchedArgs a) {
         __syncthreads();
     }
 
-    // 5. objectives, split over the cluster
-    const double N0 = __dmul_rn((double)B, (double)(ml + 1));
+    // 5. objectives, split over the cluster (costs of the slice from csl)
     auto tau_at = [&](int K) -> double { return prog_value(K == 0 ? base : key[K - 1]); };
-    auto obj_at = [&](int K) -> double { return __ddiv_rn(tau_at(K), cost_at(__dadd_rn(N0, (double)K), a)); };
+    auto obj_at = [&](int K) -> double { return __ddiv_rn(tau_at(K), csl[K - k_lo]); };
+    const int k_hi = k_lo + ccnt;
     uint64_t bv = 0;
     int bi = 0x7fffffff;
     if (a.mode == SPEC_SCHED_EXACT) {
-        const int tot = nc + 1, cpc = (tot + CL - 1) / CL;
-        const int k_lo = min(tot, rank * cpc), k_hi = min(tot, k_lo + cpc);
         for (int K = k_lo + tid; K < k_hi; K += kSchedThreads) {
             const uint64_t v = obj_bits(obj_at(K));
             if (v > bv || (v == bv && K < bi)) {
@@ -404,10 +422,10 @@ __global__ void __launch_bounds__(kSchedThreads, 1) k_schedule(SchedArgs a) {
             }
         }
     } else if (a.mode == SPEC_SCHED_ALGORITHM1) {
-        // the first valid candidate i that does not strictly improve tau / C
-        const int np = s_npos, cpc = (np + CL - 1) / CL;
-        const int i_lo = min(np, rank * cpc), i_hi = min(np, i_lo + cpc);
-        for (int i = i_lo + tid; i < i_hi; i += kSchedThreads)
+        // the first valid candidate i (i < npos) that does not strictly
+        // improve tau / C, over this CTA's slice
+        const int i_hi = min(s_npos, k_hi);
+        for (int i = k_lo + tid; i < i_hi; i += kSchedThreads)
             if (!(obj_at(i + 1) > obj_at(i)) && i < bi) bi = i;
     } else if (rank == 0 && warp == 0) {
         // D-cut: K_i = max(N0, ceil(rho_i * B(gamma+1))) for the nk ratios
@@ -520,8 +538,10 @@ namespace {
 
 // Dynamic shared memory of k_schedule for a padded candidate count (the
 // ranked path keeps the survivals in rank order in a second array).
-size_t sched_smem_bytes(int npad, int nc) {
-    return (size_t)npad * 10 + (size_t)kSchedThreads * 16 + 16 + (nc <= kRankMax ? (size_t)npad * 8 : 0);
+size_t sched_smem_bytes(int npad, int nc, int cl) {
+    const size_t cpc = (size_t)(nc + 1 + cl - 1) / cl;
+    return (size_t)npad * 10 + (size_t)kSchedThreads * 16 + 16 + (nc <= kRankMax ? (size_t)npad * 8 : 0) +
+           (cpc + 1) * 8;
 }
 
 // Cluster size of k_schedule per device: 16 CTAs where the GPU can place such
@@ -533,7 +553,7 @@ int sched_cluster_size(int dev) {
     if (g_sched_cluster[dev]) return g_sched_cluster[dev];
     int npad_max = 32;
     while (npad_max < SPEC_MAX_SCHED_CANDIDATES) npad_max <<= 1;
-    const size_t smem_max = sched_smem_bytes(npad_max, SPEC_MAX_SCHED_CANDIDATES);
+    const size_t smem_max = sched_smem_bytes(npad_max, SPEC_MAX_SCHED_CANDIDATES, 8);
     if (cudaFuncSetAttribute((const void*)k_schedule, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem_max) != cudaSuccess)
         return 0;
@@ -627,7 +647,7 @@ int spec_schedule(const float* confidence, int B, int gamma, const spec_cost_tab
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cl);
     cfg.blockDim = dim3(kSchedThreads);
-    cfg.dynamicSmemBytes = sched_smem_bytes(npad, a.nc);
+    cfg.dynamicSmemBytes = sched_smem_bytes(npad, a.nc, cl);
     cfg.stream = (cudaStream_t)stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
