@@ -25,8 +25,8 @@
 //                two-float sums), runs the accept tests with one warp ballot,
 //                writes the accepted prefix; at T > 0 sums the draw weights of
 //                the 1-2 draw rows per chunk across the cluster and draws the
-//                token by inverse CDF (fp64 prefix over chunk totals, then a
-//                scan inside the chosen chunk).
+//                token by inverse CDF over two-float prefixes (chunk totals,
+//                then the chosen chunk's segments and elements).
 #include <math.h>
 
 #include <algorithm>
