@@ -118,6 +118,57 @@ def test_worked_example_through_logits():
 
 
 # ------------------------------------------------------------------ statistics
+def _softmax64(z, T):
+    """softmax(z / T) in fp64, with T the fp32 temperature widened."""
+    y = z.astype(np.float64) / float(np.float32(T))
+    e = np.exp(y - y.max(axis=-1, keepdims=True))
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("T,V", [(0.6, 7), (1.0, 300), (1.7, 2049)])
+def test_logit_path_against_overlap_identity(dtype, T, V):
+    """Through the logit path: p(x) and q(x) agree with a softmax computed here
+    in fp64; the accept decisions are the first u * q(x) >= p(x); at a rejection
+    the residual mass is sum max(p - q, 0) = 1 - sum min(p, q) (total variation,
+    AngelSpec eqs. (4)-(5)); after full acceptance the bonus weights sum to 1.
+    All to 1e-12."""
+    rng = np.random.default_rng(int(V * 10 + T * 10) + (dtype == "bf16"))
+    B, gamma = 96, 3
+    zt32 = rng.normal(0.0, 2.0, (B, gamma + 1, V)).astype(np.float32)
+    zd32 = (zt32[:, :gamma] + rng.normal(0.0, 1.0, (B, gamma, V))).astype(np.float32)
+    if dtype == "bf16":
+        zt, zd = specsynth.to_bf16_bits(zt32), specsynth.to_bf16_bits(zd32)
+        zt32, zd32 = specsynth.bf16_bits_to_f32(zt), specsynth.bf16_bits_to_f32(zd)
+    else:
+        zt, zd = zt32, zd32
+    P, Q = _softmax64(zt32, T), _softmax64(zd32, T)
+    x = np.array([[rng.choice(V, p=Q[b, j]) for j in range(gamma)] for b in range(B)], np.int32)
+    u = rng.uniform(0.0, 1.0, (B, gamma + 2)).astype(np.float32)
+    r = oracle.verify(zt, zd, dtype, x, None, T, u)
+    assert r["rc"] == 0 and (r["status"] == 0).all()
+    n = r["accept_len"]
+    rejected = 0
+    for b in range(B):
+        px = P[b, np.arange(gamma), x[b]]
+        qx = Q[b, np.arange(gamma), x[b]]
+        assert np.allclose(r["px"][b], px, rtol=1e-12, atol=0)
+        assert np.allclose(r["qx"][b], qx, rtol=1e-12, atol=0)
+        lhs = u[b, :gamma].astype(np.float64) * qx
+        assert np.abs(lhs - px).min() > 1e-12 * px.max()  # no near-tie in these draws
+        rej = np.flatnonzero(lhs >= px)
+        want = int(rej[0]) if rej.size else gamma
+        assert n[b] == want
+        if want < gamma:
+            rejected += 1
+            tv = np.maximum(P[b, want] - Q[b, want], 0.0).sum()
+            assert abs(r["resid_mass"][b] - tv) < 1e-12
+            assert abs(r["resid_mass"][b] - (1.0 - np.minimum(P[b, want], Q[b, want]).sum())) < 1e-12
+        else:
+            assert abs(r["resid_mass"][b] - 1.0) < 1e-12
+    assert 0 < rejected < B
+
+
 def _dirichlet_rows(rng, rows, V, conc=1.0):
     return rng.dirichlet(np.full(V, conc), size=rows)
 
