@@ -283,6 +283,31 @@ def time_schedulers(sv, dev, stream, rank: int):
             "kernel_launches_per_call": 1, "modes": res}
 
 
+def graph_us_per_call(dev, stream, call, n_calls: int = 50, reps: int = 5) -> float:
+    """Device time per call: n_calls calls (call(i) for i in range(n_calls))
+    captured in one CUDA graph on a side stream, replayed reps times between
+    CUDA events."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            for i in range(n_calls):
+                call(i)
+    stream.wait_stream(side)
+    g.replay()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(side):
+        e0.record(side)
+        for _ in range(reps):
+            g.replay()
+        e1.record(side)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) * 1e3 / (reps * n_calls)
+
+
 def time_other_workloads(sv, specsynth, dev, stream, rank: int):
     """Device time per call of the other verification workloads (the small
     ones are latency-bound): 100 calls captured in a CUDA graph and replayed,
@@ -368,26 +393,33 @@ def time_packed_step(sv, specsynth, case, t, d, x, u, dev, stream, rank: int, st
     di = np.concatenate([b * gamma + np.arange(vl_h[b]) for b in range(B)])
     tp = t.view(B * (gamma + 1), V)[torch.from_numpy(ti).to(dev)].contiguous()
     dp = d.view(B * gamma, V)[torch.from_numpy(di).to(dev)].contiguous()
+    # copies of the packed logits, so that the graph-replayed steps' working
+    # set exceeds twice the L2
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    n_sets = max(1, min(8, -(-2 * l2 // (tp.nbytes + dp.nbytes))))
+    psets = [(tp, dp)] + [(tp.clone(), dp.clone()) for _ in range(n_sets - 1)]
     assert (tr_h == np.concatenate([[0], np.cumsum(vl_h + 1)[:-1]])).all()
     out_t = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
     out_n = torch.empty((B,), dtype=torch.int32, device=dev)
     ws = sv.alloc_verify_workspace(B, gamma, V, sv.BF16, dev)
 
-    def step():
+    def step(i=0):
+        ptp, pdp = psets[i % n_sets]
         sv.schedule(conf, (ratios, costs), 0, sv.SCHED_DCUT, out_verify_len=vl, workspace=sws)
         sv.pack_rows(vl, gamma, target_row=tr, draft_row=dr, totals=tot)
-        sv.verify_packed(tp, dp, tr, dr, x, vl, case.T, u, out_tokens=out_t, out_accept_len=out_n, workspace=ws)
+        sv.verify_packed(ptp, pdp, tr, dr, x, vl, case.T, u, out_tokens=out_t, out_accept_len=out_n, workspace=ws)
 
-    for _ in range(3):
-        step()
+    for i in range(3):
+        step(i)
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(steps):
-        step()
+    for i in range(steps):
+        step(i)
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    ms = e0.elapsed_time(e1) / steps
+    host_ms = e0.elapsed_time(e1) / steps
+    ms = graph_us_per_call(dev, stream, step) / 1e3
     if sv.read_status(ws) != 0 or sv.read_status(sws) != 0:
         raise RuntimeError("device status on the packed step")
     rows = int(vl_h.sum())
@@ -396,7 +428,9 @@ def time_packed_step(sv, specsynth, case, t, d, x, u, dev, stream, rank: int, st
                         f"verify of the {WORKLOAD} logits packed as [{Kt}, V] target and [{Kd}, V] draft rows",
             "ms_per_step": ms, "verified_rows_per_step": rows, "verified_rows_per_s": rows / (ms / 1e3),
             "packed_logit_bytes": logit_bytes, "logit_gbs": logit_bytes / (ms / 1e3) / 1e9,
-            "steps": steps, "kernel_launches_per_step": 2 + sv.kernel_count(B, case.T)}
+            "timing": f"50 steps in a CUDA graph, 5 replays; packed logits rotated over {n_sets} copies",
+            "host_launched_ms_per_step": host_ms, "host_launched_steps": steps,
+            "kernel_launches_per_step": 2 + sv.kernel_count(B, case.T)}
 
 
 def run_ours(args):
@@ -492,28 +526,37 @@ def run_ours(args):
     ws_s = torch.zeros(256, dtype=torch.uint8, device=dev)
     cost_s = specsynth.COST_TABLES["Bprime"]
 
-    def sched_step():
-        sv.schedule(conf_s, cost_s, specsynth.SCHED_MIN_LEN, sv.SCHED_EXACT, out_verify_len=vl_s, workspace=ws_s)
-        sv.verify(t, d, x, vl_s, case.T, u, out_tokens=out_t, out_accept_len=out_n, workspace=ws)
+    # a second copy of the logits: the graph-replayed steps alternate between
+    # the two, so the rows read in consecutive steps are not L2-resident
+    ssets = [(t, d), (t.clone(), d.clone())]
 
-    for _ in range(3):
-        sched_step()
+    def sched_step(i=0):
+        st_, sd_ = ssets[i % 2]
+        sv.schedule(conf_s, cost_s, specsynth.SCHED_MIN_LEN, sv.SCHED_EXACT, out_verify_len=vl_s, workspace=ws_s)
+        sv.verify(st_, sd_, x, vl_s, case.T, u, out_tokens=out_t, out_accept_len=out_n, workspace=ws)
+
+    for i in range(3):
+        sched_step(i)
     torch.cuda.synchronize(dev)
     s_steps = max(3, min(args.steps, 500))
     s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s0.record(stream)
-    for _ in range(s_steps):
-        sched_step()
+    for i in range(s_steps):
+        sched_step(i)
     s1.record(stream)
     torch.cuda.synchronize(dev)
-    s_ms = s0.elapsed_time(s1) / s_steps
+    s_host_ms = s0.elapsed_time(s1) / s_steps
+    s_ms = graph_us_per_call(dev, stream, sched_step) / 1e3
+    del ssets
     s_rows = int(vl_s.sum().item())
     if sv.read_status(ws) != 0 or sv.read_status(ws_s) != 0:
         raise RuntimeError("device status on the scheduled workload")
     scheduled_step = {"workload": "schedule (exact scan, cost table B', min_len 1) then verify of the "
                                   f"{WORKLOAD} logits at the scheduled lengths",
                       "ms_per_step": s_ms, "verified_rows_per_step": s_rows,
-                      "verified_rows_per_s": s_rows / (s_ms / 1e3), "steps": s_steps,
+                      "verified_rows_per_s": s_rows / (s_ms / 1e3),
+                      "timing": "50 steps in a CUDA graph, 5 replays; logits alternate between two copies",
+                      "host_launched_ms_per_step": s_host_ms, "host_launched_steps": s_steps,
                       "kernel_launches_per_step": 1 + sv.kernel_count(B, case.T)}
     sched = time_schedulers(sv, dev, stream, rank)
     packed_step = time_packed_step(sv, specsynth, case, t, d, x, u, dev, stream, rank, s_steps)
