@@ -35,6 +35,8 @@ sys.path.insert(0, ROOT)
 METRIC = "verified rows/sec at B=64,γ=16,V=128k bf16; achieved HBM GB/s as % of GB300 peak"
 UNIT = "verified rows/s"
 WORKLOAD = "block_diffusion"
+SEED_OFFSET = 0           # --seed-offset
+COST_READING = "Bprime"   # --cost-table
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "row_stats_block_diffusion.md")
 KERNEL_SOURCES = ["speculative_decoding_verification_softmax_gb300/csrc/specv_rowstats.cuh",
                   "speculative_decoding_verification_softmax_gb300/csrc/specv_common.cuh"]
@@ -191,7 +193,9 @@ def run_reference(args):
     if rank != 0:
         return
     import specsynth
-    case = specsynth.make_verify_case(WORKLOAD)
+    o = SEED_OFFSET
+    case = specsynth.make_verify_case(WORKLOAD, seed_logits=300 + o, seed_noise=301 + o, seed_tokens=302 + o,
+                                      seed_uniforms=303 + o)
     cores = os.cpu_count() or 1
     per_step = min(case.B, cores)
     W = max(args.warmup, 0)
@@ -230,12 +234,12 @@ def time_schedulers(sv, dev, stream, rank: int):
     CUDA graph, replayed, timed with CUDA events on the launching stream."""
     import torch
     import specsynth
-    conf = specsynth.make_confidences(seed=specsynth.SCHED_SEED + 1000 * rank)
+    conf = specsynth.make_confidences(seed=specsynth.SCHED_SEED + 1000 * rank + SEED_OFFSET)
     B, gamma = conf.shape
     c = torch.from_numpy(conf).to(dev)
     out = torch.empty((B,), dtype=torch.int32, device=dev)
     ws = torch.zeros(256, dtype=torch.uint8, device=dev)
-    cost = specsynth.COST_TABLES["Bprime"]
+    cost = specsynth.COST_TABLES[COST_READING]
     ratios, rcost = [0.25, 0.5, 0.75, 1.0], [10.0, 13.0, 16.0, 19.0]
     sts = np.linspace(0.8, 1.6, gamma).astype(np.float32)
     ml = specsynth.SCHED_MIN_LEN
@@ -277,7 +281,7 @@ def time_schedulers(sv, dev, stream, rank: int):
         if sv.read_status(ws) != 0:
             raise RuntimeError(f"scheduler status after replay ({name})")
     return {"workload": f"scheduled ragged: B={B}, gamma={gamma} confidences sigmoid(N(1.5, 1)), "
-                        f"min_len={ml}; cost table 8 ms + 0.02 ms/token to 512 tokens, 20 ms above; "
+                        f"min_len={ml}; cost table reading {COST_READING} of 8 ms + 0.02 ms/token, +12 ms above 512 tokens; "
                         f"D-cut ratios {ratios} with costs {rcost} ms; STS temperatures 0.8..1.6",
             "timing": f"{SCHED_REPLAYS} calls per CUDA graph, 5 replays, CUDA events",
             "kernel_launches_per_call": 1, "modes": res}
@@ -374,8 +378,8 @@ def time_packed_step(sv, specsynth, case, t, d, x, u, dev, stream, rank: int, st
     import math
     import torch
     B, gamma, V = case.B, case.gamma, case.V
-    conf = torch.from_numpy(specsynth.make_confidences(seed=specsynth.SCHED_SEED + 1000 * rank)).to(dev)
-    kt, kc = specsynth.COST_TABLES["Bprime"]
+    conf = torch.from_numpy(specsynth.make_confidences(seed=specsynth.SCHED_SEED + 1000 * rank + SEED_OFFSET)).to(dev)
+    kt, kc = specsynth.COST_TABLES[COST_READING]
     ratios = [0.25, 0.5, 0.75, 1.0]
     budgets = [max(B, math.ceil(r * B * (gamma + 1))) for r in ratios]
     costs = [float(np.interp(k, kt, kc)) for k in budgets]
@@ -447,8 +451,9 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     sv.build()
 
-    case = specsynth.make_verify_case(WORKLOAD, seed_logits=300 + 1000 * rank, seed_noise=301 + 1000 * rank,
-                                      seed_tokens=302 + 1000 * rank, seed_uniforms=303 + 1000 * rank)
+    o = 1000 * rank + SEED_OFFSET
+    case = specsynth.make_verify_case(WORKLOAD, seed_logits=300 + o, seed_noise=301 + o, seed_tokens=302 + o,
+                                      seed_uniforms=303 + o)
     B, gamma, V = case.B, case.gamma, case.V
     t, d, x, vl, u = H.to_device(case, dev)
     out_t = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
@@ -521,10 +526,10 @@ def run_ours(args):
 
     # the whole path on the scheduled ragged workload: spec_schedule (exact
     # scan, cost table B', min_len 1) feeding spec_verify, back to back
-    conf_s = torch.from_numpy(specsynth.make_confidences(seed=specsynth.SCHED_SEED + 1000 * rank)).to(dev)
+    conf_s = torch.from_numpy(specsynth.make_confidences(seed=specsynth.SCHED_SEED + 1000 * rank + SEED_OFFSET)).to(dev)
     vl_s = torch.empty((B,), dtype=torch.int32, device=dev)
     ws_s = torch.zeros(256, dtype=torch.uint8, device=dev)
-    cost_s = specsynth.COST_TABLES["Bprime"]
+    cost_s = specsynth.COST_TABLES[COST_READING]
 
     # a second copy of the logits: the graph-replayed steps alternate between
     # the two, so the rows read in consecutive steps are not L2-resident
@@ -551,7 +556,7 @@ def run_ours(args):
     s_rows = int(vl_s.sum().item())
     if sv.read_status(ws) != 0 or sv.read_status(ws_s) != 0:
         raise RuntimeError("device status on the scheduled workload")
-    scheduled_step = {"workload": "schedule (exact scan, cost table B', min_len 1) then verify of the "
+    scheduled_step = {"workload": f"schedule (exact scan, cost table {COST_READING}, min_len 1) then verify of the "
                                   f"{WORKLOAD} logits at the scheduled lengths",
                       "ms_per_step": s_ms, "verified_rows_per_step": s_rows,
                       "verified_rows_per_s": s_rows / (s_ms / 1e3),
@@ -727,7 +732,7 @@ def run_profile_sched(args):
     out = torch.empty((conf.shape[0],), dtype=torch.int32, device="cuda")
     ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
     for _ in range(args.warmup + args.steps):
-        sv.schedule(conf, specsynth.COST_TABLES["Bprime"], specsynth.SCHED_MIN_LEN, sv.SCHED_EXACT,
+        sv.schedule(conf, specsynth.COST_TABLES[COST_READING], specsynth.SCHED_MIN_LEN, sv.SCHED_EXACT,
                     out_verify_len=out, workspace=ws)
     torch.cuda.synchronize()
     st = sv.read_status(ws)
@@ -748,7 +753,13 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--seed-offset", type=int, default=0,
+                    help="added to every seed of the synthetic inputs (default 0: the stated recipe)")
+    ap.add_argument("--cost-table", choices=["Bprime", "A", "C"], default="Bprime",
+                    help="reading of the round-cost table used by the scheduled legs")
     args = ap.parse_args(argv)
+    global SEED_OFFSET, COST_READING
+    SEED_OFFSET, COST_READING = args.seed_offset, args.cost_table
     if args.profile_case:
         run_profile_case(args)
     elif args.profile_sched:

@@ -54,7 +54,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     """Compile csrc/*.cu for sm_103a into libspecv.so (in-tree, parallel TUs)."""
     srcs = [os.path.join(_CSRC, s) for s in SOURCES]
     deps = srcs + [os.path.join(_CSRC, "specv_common.cuh"), os.path.join(_CSRC, "specv_rowstats.cuh"),
-                   os.path.join(_ROOT, "include", "specv.h")]
+                   os.path.join(_CSRC, "specv_trace.h"), os.path.join(_ROOT, "include", "specv.h")]
     if (not force and os.path.exists(LIB_PATH)
             and all(os.path.getmtime(LIB_PATH) >= os.path.getmtime(d) for d in deps)):
         return LIB_PATH

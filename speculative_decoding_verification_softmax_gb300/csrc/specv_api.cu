@@ -5,6 +5,7 @@
 #include <vector>
 
 #include "specv_common.cuh"
+#include "specv_trace.h"
 
 extern "C" {
 
@@ -56,6 +57,7 @@ extern "C" int spec_selftest_wait(long long limit_ns, int32_t* status, unsigned 
 // Sequential Temperature Scaling fit on the host ("UraionSpec" §2.4, §3.6).
 int spec_sts_fit(const float* confidence, const int32_t* accept_len, int n, int gamma, float* out_temperature,
                  double* out_ece) {
+    specv::TraceRange tr("spec_sts_fit");
     if (n < 1 || gamma < 1 || gamma > SPEC_MAX_GAMMA) return SPEC_ERR_SHAPE;
     if (!confidence || !accept_len || !out_temperature) return SPEC_ERR_NULL;
     for (long long i = 0; i < (long long)n * gamma; ++i)

@@ -32,6 +32,7 @@
 #include <stdint.h>
 
 #include "specv_common.cuh"
+#include "specv_trace.h"
 
 namespace cg = cooperative_groups;
 
@@ -602,6 +603,7 @@ static bool sts_ok(const float* T, int gamma) {
 int spec_schedule(const float* confidence, int B, int gamma, const spec_cost_table* cost, int min_len,
                   spec_sched_mode mode, const float* sts_temperature, int32_t* out_verify_len, void* workspace,
                   size_t workspace_bytes, spec_stream_t stream) {
+    TraceRange tr("spec_schedule");
     if (B < 0 || B > SPEC_MAX_BATCH || gamma < 0 || gamma > SPEC_MAX_GAMMA || min_len < 0 || min_len > gamma)
         return SPEC_ERR_SHAPE;
     if ((long long)B * (gamma - min_len) > SPEC_MAX_SCHED_CANDIDATES) return SPEC_ERR_SHAPE;
@@ -663,6 +665,7 @@ int spec_schedule(const float* confidence, int B, int gamma, const spec_cost_tab
 int spec_schedule_static(const float* confidence, int B, int gamma, float threshold, int max_len, int min_len,
                          const float* sts_temperature, int32_t* out_verify_len, void* workspace,
                          size_t workspace_bytes, spec_stream_t stream) {
+    TraceRange tr("spec_schedule_static");
     if (B < 0 || B > SPEC_MAX_BATCH || gamma < 0 || gamma > SPEC_MAX_GAMMA || min_len < 0 || min_len > max_len ||
         max_len > gamma)
         return SPEC_ERR_SHAPE;

@@ -35,6 +35,7 @@
 #include <cooperative_groups.h>
 
 #include "specv_rowstats.cuh"
+#include "specv_trace.h"
 
 namespace cg = cooperative_groups;
 
@@ -1034,6 +1035,7 @@ int spec_verify(const void* target_logits, const void* draft_logits, spec_dtype 
                 int V, const int32_t* draft_tokens, const int32_t* verify_len, float temperature,
                 const float* uniforms, int32_t* out_tokens, int32_t* out_accept_len, void* workspace,
                 size_t workspace_bytes, spec_stream_t stream) {
+    TraceRange tr("spec_verify");
     return verify_impl(target_logits, draft_logits, RowMap{nullptr, nullptr, 0, 0}, dt, B, gamma, V, draft_tokens,
                        verify_len, temperature, uniforms, out_tokens, out_accept_len, workspace, workspace_bytes,
                        stream);
@@ -1044,6 +1046,7 @@ int spec_verify_packed(const void* target_logits, int K_target, const void* draf
                        const int32_t* draft_tokens, const int32_t* verify_len, float temperature,
                        const float* uniforms, int32_t* out_tokens, int32_t* out_accept_len, void* workspace,
                        size_t workspace_bytes, spec_stream_t stream) {
+    TraceRange tr("spec_verify_packed");
     if (K_target < 0 || K_draft < 0) return SPEC_ERR_SHAPE;
     if (B > 0) {
         if (!target_row) return SPEC_ERR_NULL;
@@ -1057,6 +1060,7 @@ int spec_verify_packed(const void* target_logits, int K_target, const void* draf
 
 int spec_pack_rows(const int32_t* verify_len, int B, int gamma, int32_t* target_row, int32_t* draft_row,
                    int32_t* totals, spec_stream_t stream) {
+    TraceRange tr("spec_pack_rows");
     if (B < 0 || B > SPEC_MAX_BATCH || gamma < 0 || gamma > SPEC_MAX_GAMMA) return SPEC_ERR_SHAPE;
     if (!totals) return SPEC_ERR_NULL;
     if (B > 0 && (!verify_len || !target_row || !draft_row)) return SPEC_ERR_NULL;
