@@ -316,7 +316,8 @@ const char* spec_status_string(int status);
 /* Registers two cudaEvent_t handles (as void*) that later spec_verify calls
  * record on their stream immediately before and after the row-statistics
  * kernel (the HBM-streaming pass), so a caller can time that kernel alone.
- * Pass NULL, NULL to stop.  Process-wide setting; not thread-safe. */
+ * Pass NULL, NULL to stop.  Process-wide setting: calls racing with it on
+ * other threads may record the old or the new pair. */
 int spec_profile_events(void* before_row_stats, void* after_row_stats);
 
 /* Number of kernels one spec_verify call launches for these arguments

@@ -30,6 +30,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include <cooperative_groups.h>
@@ -891,7 +892,9 @@ using namespace specv;
 
 namespace {
 
-cudaEvent_t g_ev_before = nullptr, g_ev_after = nullptr;
+// profiling hook (spec_profile_events): atomics, so that setting it from one
+// thread while another launches is not a data race
+std::atomic<cudaEvent_t> g_ev_before{nullptr}, g_ev_after{nullptr};
 
 struct DeviceInfo {
     int sms = 0;
@@ -941,7 +944,9 @@ int launch_chain(const StatsArgs& sa, const FinishArgs& fa, const Layout& L, int
     const long long max_items = (long long)L.R * L.nch;
     const int grid = (int)std::min<long long>(sms, (max_items + kStatsWarps - 1) / kStatsWarps);
     const bool packed = sa.rm.trow != nullptr;
-    if (g_ev_before) cudaEventRecord(g_ev_before, st);
+    const cudaEvent_t ev_before = g_ev_before.load(std::memory_order_relaxed);
+    const cudaEvent_t ev_after = g_ev_after.load(std::memory_order_relaxed);
+    if (ev_before) cudaEventRecord(ev_before, st);
     if (aligned_rows) {
         if (packed) k_row_stats<ES, GREEDY, true, true><<<grid, kStatsThreads, kStatsSmem, st>>>(sa, L);
         else k_row_stats<ES, GREEDY, true, false><<<grid, kStatsThreads, kStatsSmem, st>>>(sa, L);
@@ -949,7 +954,7 @@ int launch_chain(const StatsArgs& sa, const FinishArgs& fa, const Layout& L, int
         if (packed) k_row_stats<ES, GREEDY, false, true><<<grid, kStatsThreads, kStatsSmem, st>>>(sa, L);
         else k_row_stats<ES, GREEDY, false, false><<<grid, kStatsThreads, kStatsSmem, st>>>(sa, L);
     }
-    if (g_ev_after) cudaEventRecord(g_ev_after, st);
+    if (ev_after) cudaEventRecord(ev_after, st);
     // one cluster per request; it may be scheduled while the streaming kernel
     // finishes and waits for its results with griddepcontrol.wait
     const int cs = finish_cluster_size(sa.B, sa.gamma, L.nch, GREEDY, sms);
@@ -1087,8 +1092,8 @@ int spec_verify_stats(const void* workspace, size_t workspace_bytes, int B, int 
 }
 
 int spec_profile_events(void* before_row_stats, void* after_row_stats) {
-    g_ev_before = (cudaEvent_t)before_row_stats;
-    g_ev_after = (cudaEvent_t)after_row_stats;
+    g_ev_before.store((cudaEvent_t)before_row_stats, std::memory_order_relaxed);
+    g_ev_after.store((cudaEvent_t)after_row_stats, std::memory_order_relaxed);
     return SPEC_OK;
 }
 
