@@ -281,13 +281,17 @@ __global__ void __launch_bounds__(kStatsThreads, 1) k_row_stats(StatsArgs a, Lay
     int* hdr = (int*)(a.ws + L.hdr);
     float2* partial = (float2*)(a.ws + L.partial);
 
-    if (blockIdx.x == 0 && tid == 0) {  // per-call reset of the status words
-        hdr[kHdrStatus] = 0;
-        hdr[kHdrEvents] = 0;
-    }
     if (lane == 0) {
         for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
         fence_mbar_init();
+    }
+    // launched as a programmatic dependent of the preceding kernel in the
+    // stream: nothing in global memory is read or written before its results
+    // are complete and visible
+    pdl_wait();
+    if (blockIdx.x == 0 && tid == 0) {  // per-call reset of the status words
+        hdr[kHdrStatus] = 0;
+        hdr[kHdrEvents] = 0;
     }
     block_row_prefix<GREEDY, PACKED>(a.verify_len, a.rm, a.B, a.gamma, prefix);
     pdl_trigger();

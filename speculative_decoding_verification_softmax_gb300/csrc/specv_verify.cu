@@ -947,12 +947,26 @@ int launch_chain(const StatsArgs& sa, const FinishArgs& fa, const Layout& L, int
     const cudaEvent_t ev_before = g_ev_before.load(std::memory_order_relaxed);
     const cudaEvent_t ev_after = g_ev_after.load(std::memory_order_relaxed);
     if (ev_before) cudaEventRecord(ev_before, st);
-    if (aligned_rows) {
-        if (packed) k_row_stats<ES, GREEDY, true, true><<<grid, kStatsThreads, kStatsSmem, st>>>(sa, L);
-        else k_row_stats<ES, GREEDY, true, false><<<grid, kStatsThreads, kStatsSmem, st>>>(sa, L);
-    } else {
-        if (packed) k_row_stats<ES, GREEDY, false, true><<<grid, kStatsThreads, kStatsSmem, st>>>(sa, L);
-        else k_row_stats<ES, GREEDY, false, false><<<grid, kStatsThreads, kStatsSmem, st>>>(sa, L);
+    {
+        // a programmatic dependent of the preceding kernel (the previous call's
+        // finish kernel, say): its CTAs are placed as that kernel drains and
+        // wait in griddepcontrol.wait instead of being launched after it
+        cudaLaunchAttribute pa[1];
+        pa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        pa[0].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t kc = {};
+        kc.gridDim = dim3((unsigned)grid);
+        kc.blockDim = dim3(kStatsThreads);
+        kc.dynamicSmemBytes = kStatsSmem;
+        kc.stream = st;
+        kc.attrs = pa;
+        kc.numAttrs = 1;
+        cudaError_t ke;
+        if (aligned_rows) ke = packed ? cudaLaunchKernelEx(&kc, k_row_stats<ES, GREEDY, true, true>, sa, L)
+                                      : cudaLaunchKernelEx(&kc, k_row_stats<ES, GREEDY, true, false>, sa, L);
+        else ke = packed ? cudaLaunchKernelEx(&kc, k_row_stats<ES, GREEDY, false, true>, sa, L)
+                         : cudaLaunchKernelEx(&kc, k_row_stats<ES, GREEDY, false, false>, sa, L);
+        if (ke != cudaSuccess) return SPEC_ERR_CUDA;
     }
     if (ev_after) cudaEventRecord(ev_after, st);
     // one cluster per request; it may be scheduled while the streaming kernel
