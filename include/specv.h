@@ -114,6 +114,12 @@ size_t spec_verify_workspace_bytes(int B, int gamma, int V, spec_dtype dt);
  * Draws use the inverse CDF: the token is the smallest v whose running sum of
  * weights exceeds u * (sum of weights).  Returns SPEC_OK or a host-detected
  * error (nothing launched).  B == 0 returns SPEC_OK without launching.
+ * Stream order: the call's kernels are programmatic dependent launches, each
+ * waiting (griddepcontrol.wait) for the work before it on `stream` before
+ * touching global memory, and each letting the next kernel be scheduled early.
+ * A caller's own kernel launched right after with programmatic stream
+ * serialization must likewise wait before reading the outputs; ordinary
+ * launches, copies and events see them complete.
  */
 int spec_verify(const void* target_logits, const void* draft_logits, spec_dtype dt, int B,
                 int gamma, int V, const int32_t* draft_tokens, const int32_t* verify_len,
