@@ -54,3 +54,41 @@ def test_interleaved_streams_match_sequential():
             tok, n, ws = res
             assert np.array_equal(tok.cpu().numpy(), seq[i][0]) and np.array_equal(n.cpu().numpy(), seq[i][1])
             assert sv.read_status(ws) == 0
+
+
+def test_inputs_written_just_before_the_call_are_seen():
+    """Stream order with the programmatic dependent launches: kernels that
+    rewrite the inputs (verify lengths, uniforms, logits) right before each
+    call on the same stream, with no host synchronisation, are seen by that
+    call; each call matches the same call run alone."""
+    import torch
+    import speculative_decoding_verification_softmax_gb300 as sv
+    sv.build()
+    case = specsynth.make_verify_case("mtp_chat", B=16, V=32000)
+    t, d, x, vl, u = H.to_device(case)
+    rng = np.random.default_rng(11)
+    vls = [torch.from_numpy(rng.integers(0, case.gamma + 1, case.B).astype(np.int32)).cuda() for _ in range(6)]
+    us = [torch.from_numpy(rng.uniform(0, 1, u.shape).astype(np.float32)).cuda() for _ in range(6)]
+    scales = [1.0, 0.5, 2.0, 1.0, 0.25, 1.5]
+    t0, d0 = t.clone(), d.clone()
+    ws = sv.alloc_verify_workspace(case.B, case.gamma, case.V, sv.BF16)
+
+    # back to back: the inputs are rewritten in place by torch kernels before each call
+    outs = []
+    for k in range(6):
+        vl.copy_(vls[k])
+        u.copy_(us[k])
+        torch.mul(t0, scales[k], out=t)
+        torch.mul(d0, scales[k], out=d)
+        tok, n, _ = sv.verify(t, d, x, vl, case.T, u, workspace=ws)
+        outs.append((tok.clone(), n.clone()))
+    torch.cuda.synchronize()
+
+    for k in range(6):
+        tk, dk = (t0 * scales[k]).contiguous(), (d0 * scales[k]).contiguous()
+        torch.cuda.synchronize()
+        tok, n, _ = sv.verify(tk, dk, x, vls[k].clone(), case.T, us[k].clone())
+        torch.cuda.synchronize()
+        assert (tok.cpu().numpy() == outs[k][0].cpu().numpy()).all(), k
+        assert (n.cpu().numpy() == outs[k][1].cpu().numpy()).all(), k
+    assert sv.read_status(ws) == 0
