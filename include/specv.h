@@ -67,7 +67,8 @@ enum {
     SPEC_ERR_TOKEN = -6,       /* device: draft token outside [0, V) at a tested position */
     SPEC_ERR_WORKSPACE = -7,   /* workspace smaller than the *_workspace_bytes value */
     SPEC_ERR_COST_TABLE = -8,  /* cost table: n outside [1, 32], knots not increasing, cost <= 0 */
-    SPEC_ERR_NONFINITE = -9,   /* device: a needed logit row has a NaN, +inf, or no finite value */
+    SPEC_ERR_NONFINITE = -9,   /* device: a needed logit row has a NaN, +inf, no finite value, or (T > 0)
+                                  a largest |z| * log2(e) / T beyond the fp32 range */
     SPEC_ERR_TIMEOUT = -10,    /* device: a bounded wait expired (results of the call invalid) */
     SPEC_ERR_CUDA = -11,       /* a CUDA runtime call failed (launch, attribute query) */
     SPEC_ERR_UNIFORM = -12,    /* device: a used uniform outside [0, 1) */

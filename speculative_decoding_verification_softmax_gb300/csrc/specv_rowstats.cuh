@@ -236,6 +236,9 @@ __device__ __forceinline__ float2 chunk_stats(const uint4* sm, int nvec_rt, int 
     if (m != m || m == INFINITY) return make_float2(__int_as_float(0x7fc00000), 0.f);
     if (m == -INFINITY) return make_float2(-INFINITY, 0.f);
     const float Mc = ceilf(fmaf(m, c_hi, m * c_lo));
+    // |max| * log2(e) / T beyond the fp32 range: no usable scale, reported
+    // like a non-finite row
+    if (!(fabsf(Mc) <= 3.0e38f)) return make_float2(__int_as_float(0x7fc00000), 0.f);
     // packed FP32x2 arithmetic: (z*c_hi - Mc) + z*c_lo for two elements per FMA
     const float2 ch2 = make_float2(c_hi, c_hi), cl2 = make_float2(c_lo, c_lo), nm2 = make_float2(-Mc, -Mc);
     float2 p0 = make_float2(0.f, 0.f), p1 = p0;

@@ -184,6 +184,33 @@ def test_invalid_inputs_marked_per_request():
     assert g["device_status"] in (sv.ERR_VERIFY_LEN, sv.ERR_TOKEN, sv.ERR_UNIFORM, sv.ERR_NONFINITE)
 
 
+@pytest.mark.parametrize("name", ["tiny", "mtp_chat"])
+def test_logit_scale_beyond_fp32_is_reported(name):
+    """At T > 0 the streaming pass keeps each chunk's scale max|z| * log2(e) / T
+    as an fp32 integer; a row where that leaves the fp32 range (here |z| = 3e38
+    at T = 1) is reported as SPEC_ERR_NONFINITE (the fp64 oracle still computes
+    it), and the other requests are unaffected."""
+    import speculative_decoding_verification_softmax_gb300 as sv
+    case = specsynth.make_verify_case(name, B=6, V=1000)
+    big = np.array([3e38, -3e38], np.float32)
+    if case.dtype == "bf16":
+        big = specsynth.to_bf16_bits(big)
+    case.target[1, 0, 5] = big[0]      # 3e38 * log2(e) / T overflows fp32 for T <= 1
+    case.draft[2, 1, :] = big[1]       # a row whose max is -3e38
+    g = H.gpu_verify(case)
+    o = H.oracle_verify(case)
+    assert g["status"][1] == sv.ERR_NONFINITE and g["status"][2] == sv.ERR_NONFINITE
+    assert g["accept_len"][1] == -1 and g["accept_len"][2] == -1
+    assert g["device_status"] == sv.ERR_NONFINITE
+    others = np.array([0, 3, 4, 5])
+    assert (g["status"][others] == 0).all() and (o["status"][others] == 0).all()
+    # the other requests against the oracle (near-ties excused as everywhere)
+    sub = {k: v[others] for k, v in o.items() if isinstance(v, np.ndarray) and v.shape[:1] == (case.B,)}
+    P = H.compare(sub, g["tokens"][others], g["accept_len"][others], g["px"][others], g["qx"][others],
+                  g["mass"][others], g["status"][others])
+    assert not P.mismatches
+
+
 def test_masked_vocabulary_entries():
     """-inf logits (masked tokens) carry zero probability and are never drawn."""
     case = specsynth.make_verify_case("mtp_chat", B=8, V=2000)
