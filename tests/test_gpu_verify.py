@@ -211,6 +211,21 @@ def test_logit_scale_beyond_fp32_is_reported(name):
     assert not P.mismatches
 
 
+@pytest.mark.parametrize("T", [1e-4, 1e-2, 5e-2, 5.0, 100.0, 1e4])
+def test_temperature_extremes(T):
+    """Parity at the ends of the temperature range, with the draft tokens drawn
+    from q at that temperature (as a drafter sampling at T would).  At small T
+    most probabilities underflow fp32 (about 1e-38 of the row's largest); the
+    tested ones do not, because the drafted tokens are likely under q and the
+    residual of a rejection sits on the target's likely tokens."""
+    case = specsynth.make_verify_case("mtp_chat", B=64, V=32000, T=T)
+    g, o, P = _run(case)
+    _report(f"T={T:g}", P)
+    assert g["device_status"] == 0
+    assert not P.mismatches
+    assert P.accept_flagged <= max(1, 1e-4 * P.positions)
+
+
 def test_masked_vocabulary_entries():
     """-inf logits (masked tokens) carry zero probability and are never drawn."""
     case = specsynth.make_verify_case("mtp_chat", B=8, V=2000)
