@@ -13,7 +13,9 @@
 //     "AngelSpec" §1).
 //   * T == 0 is greedy: accept while x_j is the target argmax.
 //
-// Kernel chain on the caller's stream (no host synchronisation):
+// Kernel chain on the caller's stream (no host synchronisation; both kernels
+// are programmatic dependent launches of the kernel before them, placed while
+// it drains and waiting in griddepcontrol.wait before touching its results):
 //   k_row_stats  persistent, one CTA per SM: the HBM pass.  Each CTA first
 //                derives the needed rows from verify_len (target 0..ell, draft
 //                0..ell-1).  Each warp then streams 4 KiB row chunks through its
