@@ -10,6 +10,7 @@ from __future__ import annotations
 import ctypes
 import os
 import subprocess
+import threading
 
 import numpy as np
 
@@ -17,6 +18,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 _lib = None
+_lock = threading.Lock()
 
 # Per-request status values (the library's error-code numbers).
 OK, ERR_SHAPE, ERR_TEMPERATURE, ERR_VERIFY_LEN, ERR_TOKEN = 0, -2, -4, -5, -6
@@ -36,6 +38,14 @@ def build(force: bool = False) -> str:
 
 def _L():
     global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:  # the test helpers call the oracle from several host threads
+        return _load()
+
+
+def _load():
+    global _lib
     if _lib is None:
         # A mutated copy of the oracle may be substituted (the pin-sensitivity
         # test plants mistakes in oracle.c and expects the pins to fail).
@@ -49,6 +59,7 @@ def _L():
         lib.oracle_verify.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, dbl, vp, vp, vp,
                                       vp, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.oracle_verify_probs.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp, vp]
+        lib.oracle_draw_cdf.argtypes = [vp, vp, i32, i32, i32, i32, vp, dbl, i32, i32, vp, i32, vp, vp]
         lib.oracle_cost_at.argtypes = [dbl, vp, vp, i32, vp]
         lib.oracle_sched_exact.argtypes = [vp, i32, i32, vp, vp, i32, i32, vp, vp, vp]
         lib.oracle_sched_alg1.argtypes = [vp, i32, i32, vp, vp, i32, i32, vp]
@@ -58,7 +69,7 @@ def _L():
         lib.oracle_sched_threshold.argtypes = [vp, i32, i32, dbl, i32, i32, vp]
         lib.oracle_sts_ece.argtypes = [vp, vp, i32, i32, vp]
         lib.oracle_sts_fit.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp]
-        for f in ("oracle_verify", "oracle_verify_probs", "oracle_cost_at", "oracle_sched_exact",
+        for f in ("oracle_verify", "oracle_verify_probs", "oracle_draw_cdf", "oracle_cost_at", "oracle_sched_exact",
                   "oracle_sched_alg1", "oracle_sched_brute", "oracle_set_sts", "oracle_sched_dcut",
                   "oracle_sched_threshold", "oracle_sts_ece", "oracle_sts_fit"):
             getattr(lib, f).restype = ctypes.c_int
@@ -102,6 +113,27 @@ def verify(target, draft, dtype: str, tokens, verify_len, T: float, uniforms, *,
                             _p(out["status"]), _p(out["events"]))
     out["rc"] = rc
     return out
+
+
+def draw_cdf(target, draft, dtype: str, verify_len, T: float, b: int, n: int, query) -> tuple:
+    """Normalised CDF edges (lo, hi) of the tokens in ``query`` in the oracle's
+    own draw for request ``b`` after ``n`` accepted drafts (the residual
+    max(p - q, 0) of row n after a rejection, else p of row verify_len[b]).
+    T > 0; arrays laid out as for :func:`verify`."""
+    B_all, G1, V = target.shape
+    gamma = G1 - 1
+    dt = 1 if dtype == "bf16" else 0
+    t = np.ascontiguousarray(target[b:b + 1])
+    d = np.ascontiguousarray(draft[b:b + 1]) if draft is not None and gamma > 0 else None
+    vl = None if verify_len is None else np.ascontiguousarray(verify_len[b:b + 1], np.int32)
+    q = np.ascontiguousarray(np.atleast_1d(query), np.int32)
+    lo = np.empty(len(q))
+    hi = np.empty(len(q))
+    rc = _L().oracle_draw_cdf(_p(t), _p(d), dt, 1, gamma, V, _p(vl), float(np.float32(T)), 0, int(n),
+                              _p(q), len(q), _p(lo), _p(hi))
+    if rc != OK:
+        raise ValueError(f"oracle_draw_cdf rejected request {b}, n={n}: {rc}")
+    return lo, hi
 
 
 def verify_probs(P, Q, tokens, uniforms) -> dict:

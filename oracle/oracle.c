@@ -153,6 +153,36 @@ static int32_t inverse_cdf(const double* w, int V, double u, double* lo, double*
 
 static int uniform_ok(float u) { return u >= 0.0f && u < 1.0f; }
 
+/* The weights of the draw that emits the token at position n of request b
+ * (n accepted drafts out of ell tested), T > 0:
+ *   n < ell : [BL] residual w = max(p_n - q_n, 0), p_n from target row n and
+ *             q_n from draft row n; if it sums to zero in floating point, w =
+ *             p_n instead (EV_RESIDUAL_EMPTY);
+ *   n == ell: the bonus draw, w = p of target row ell ([AS] §1, §4.1).
+ * p, q: scratch of V doubles.  Returns the uniform slot of the draw (gamma for
+ * the residual, gamma + 1 for the bonus). */
+static int draw_weights(const void* target, const void* draft, int dtype, int b, int gamma, int V, int n,
+                        int ell, double T, double* p, double* q, double* w, int* ev) {
+    const int G1 = gamma + 1;
+    row_softmax(target, dtype, ((int64_t)b * G1 + n) * V, V, T, p);
+    if (n < ell) {
+        row_softmax(draft, dtype, ((int64_t)b * gamma + n) * V, V, T, q);
+        double W = 0.0;
+        for (int v = 0; v < V; ++v) {
+            double d = p[v] - q[v];
+            w[v] = d > 0.0 ? d : 0.0;
+            W += w[v];
+        }
+        if (!(W > 0.0)) {
+            *ev |= EV_RESIDUAL_EMPTY;
+            for (int v = 0; v < V; ++v) w[v] = p[v];
+        }
+        return gamma;
+    }
+    for (int v = 0; v < V; ++v) w[v] = p[v];
+    return gamma + 1;
+}
+
 /* -------------------------------------------------------------- verification
  * Batched lossless verification, one request at a time.
  *
@@ -256,27 +286,8 @@ int oracle_verify(const void* target, const void* draft, int dtype, int B, int g
                 for (int j = 0; j < n; ++j) ot[j] = x[j];
 
                 /* The emitted token at position n. */
-                double ud;
-                row_softmax(target, dtype, ((int64_t)b * G1 + n) * V, V, T, p);
-                if (n < ell) {
-                    /* [BL] residual: w = max(p_n - q_n, 0) */
-                    row_softmax(draft, dtype, ((int64_t)b * gamma + n) * V, V, T, q);
-                    double W = 0.0;
-                    for (int v = 0; v < V; ++v) {
-                        double d = p[v] - q[v];
-                        w[v] = d > 0.0 ? d : 0.0;
-                        W += w[v];
-                    }
-                    if (!(W > 0.0)) {
-                        ev |= EV_RESIDUAL_EMPTY;
-                        for (int v = 0; v < V; ++v) w[v] = p[v];
-                    }
-                    ud = (double)u[gamma];
-                } else {
-                    /* bonus token from p of target row ell */
-                    for (int v = 0; v < V; ++v) w[v] = p[v];
-                    ud = (double)u[gamma + 1];
-                }
+                const int slot = draw_weights(target, draft, dtype, b, gamma, V, n, ell, T, p, q, w, &ev);
+                const double ud = (double)u[slot];
                 double lo = NAN, hi = NAN, W = 0.0;
                 for (int v = 0; v < V; ++v) W += w[v];
                 int32_t tok = inverse_cdf(w, V, ud, &lo, &hi, &ev);
@@ -298,6 +309,47 @@ int oracle_verify(const void* target, const void* draft, int dtype, int B, int g
     free(p);
     free(q);
     free(w);
+    return OR_OK;
+}
+
+/* Normalised CDF edges of queried tokens in the oracle's own draw for request
+ * b, given n accepted drafts out of the request's verify length: for token t,
+ * lo = (w_0 + ... + w_{t-1}) / W and hi = (w_0 + ... + w_t) / W, with the
+ * weights of draw_weights ([BL] residual or the bonus p) and the same
+ * left-to-right fp64 sums as the draw itself, W their total.  A draw with
+ * uniform u emits t exactly when lo <= u < hi (up to the last-positive-bin
+ * rule), so the distance from u to [lo, hi] says how far u is from a value at
+ * which t would be the correct token.  T > 0; inputs laid out as for
+ * oracle_verify; request b must be valid.  Returns OR_OK or OR_ERR_SHAPE. */
+int oracle_draw_cdf(const void* target, const void* draft, int dtype, int B, int gamma, int V,
+                    const int32_t* verify_len, double T, int b, int n, const int32_t* query, int nq,
+                    double* lo, double* hi) {
+    if (b < 0 || b >= B || gamma < 0 || gamma > 63 || V < 1 || !(T > 0.0)) return OR_ERR_SHAPE;
+    const int ell = verify_len ? verify_len[b] : gamma;
+    if (ell < 0 || ell > gamma || n < 0 || n > ell) return OR_ERR_SHAPE;
+    double* p = (double*)malloc(sizeof(double) * (size_t)V);
+    double* q = (double*)malloc(sizeof(double) * (size_t)V);
+    double* w = (double*)malloc(sizeof(double) * (size_t)V);
+    double* cum = (double*)malloc(sizeof(double) * ((size_t)V + 1));
+    if (!p || !q || !w || !cum) { free(p); free(q); free(w); free(cum); return OR_ERR_SHAPE; }
+    int ev = 0;
+    draw_weights(target, draft, dtype, b, gamma, V, n, ell, T, p, q, w, &ev);
+    cum[0] = 0.0;
+    for (int v = 0; v < V; ++v) cum[v + 1] = cum[v] + w[v];
+    const double W = cum[V];
+    for (int i = 0; i < nq; ++i) {
+        const int t = query[i];
+        if (t < 0 || t >= V) {
+            lo[i] = hi[i] = NAN;
+        } else {
+            lo[i] = cum[t] / W;
+            hi[i] = cum[t + 1] / W;
+        }
+    }
+    free(p);
+    free(q);
+    free(w);
+    free(cum);
     return OR_OK;
 }
 

@@ -302,3 +302,21 @@ def make_replicated_case(P: np.ndarray, Q: np.ndarray, B: int, seed_tokens: int,
     vl = np.full(B, gamma if verify_len is None else verify_len, np.int32)
     spec = VerifySpec("replicated", B, gamma, V, dtype, T, 0.0, 0.0)
     return VerifyCase(spec, target, draft, tokens, vl, uniforms)
+
+
+def to_device(case: VerifyCase, device="cuda"):
+    """The case's arrays as torch tensors on ``device`` (bf16 bits reinterpreted
+    as torch.bfloat16): target, draft, draft tokens, verify lengths, uniforms.
+    Marshalling only; torch is imported here so that the generators above work
+    without it."""
+    import torch
+    if case.dtype == "bf16":
+        t = torch.from_numpy(case.target.view(np.int16)).to(device).view(torch.bfloat16)
+        d = torch.from_numpy(case.draft.view(np.int16)).to(device).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(case.target).to(device)
+        d = torch.from_numpy(case.draft).to(device)
+    x = torch.from_numpy(case.draft_tokens).to(device)
+    vl = torch.from_numpy(case.verify_len).to(device)
+    u = torch.from_numpy(case.uniforms).to(device)
+    return t, d, x, vl, u

@@ -17,15 +17,16 @@ SRC = os.path.join(ROOT, "oracle", "oracle.c")
 MUTATIONS = {
     "accept_test_transposed": ("if (uj * qxv[n] < pxv[n]) ++n;", "if (uj * pxv[n] < qxv[n]) ++n;"),
     "residual_sign_flipped": ("double d = p[v] - q[v];", "double d = q[v] - p[v];"),
-    "bonus_uses_residual_slot": ("ud = (double)u[gamma + 1];", "ud = (double)u[gamma];"),
+    "bonus_uses_residual_slot": ("w[v] = p[v];\n    return gamma + 1;", "w[v] = p[v];\n    return gamma;"),
     "emitted_row_shifted": ("row_softmax(target, dtype, ((int64_t)b * G1 + n) * V, V, T, p);\n"
-                            "                if (n < ell)",
+                            "    if (n < ell)",
                             "row_softmax(target, dtype, ((int64_t)b * G1 + (n > 0 ? n - 1 : 0)) * V, V, T, p);\n"
-                            "                if (n < ell)"),
+                            "    if (n < ell)"),
     "residual_draft_row_shifted": ("row_softmax(draft, dtype, ((int64_t)b * gamma + n) * V, V, T, q);\n"
-                                   "                    double W",
+                                   "        double W",
                                    "row_softmax(draft, dtype, ((int64_t)b * gamma + (n > 0 ? n - 1 : 0)) * V, V, T, q);\n"
-                                   "                    double W"),
+                                   "        double W"),
+    "draw_cdf_edge_shifted": ("lo[i] = cum[t] / W;", "lo[i] = cum[t > 0 ? t - 1 : 0] / W;"),
     "temperature_ignored": ("double y = logit_at(base, dtype, off + v) / T;",
                             "double y = logit_at(base, dtype, off + v) / 1.0;"),
     "softmax_not_normalised": ("for (int v = 0; v < V; ++v) p[v] = p[v] / S;",

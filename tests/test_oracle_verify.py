@@ -117,6 +117,45 @@ def test_worked_example_through_logits():
     np.testing.assert_allclose(r["resid_mass"][1:3], 0.2, atol=1e-7)
 
 
+def test_draw_cdf_edges_of_the_worked_example():
+    """The oracle's CDF lookup on the page's example: after the rejection of
+    token 1 the normalised residual is [0.5, 0, 0.5], so the bins are [0, .5),
+    the empty [.5, .5) and [.5, 1); after acceptance the bonus draw uses p =
+    [.5, .3, .2], bins [0, .5), [.5, .8), [.8, 1).  fp32 logits: 1e-6."""
+    g = _worked()
+    p, q = np.array(g["p_target"]), np.array(g["q_draft"])
+    c = specsynth.make_replicated_case(np.array([p, p]), np.array([q]), 2, 11, 12)
+    c.draft_tokens[:] = 1
+    c.uniforms[:] = np.array([[0.61, 0.49, 0.5], [0.2, 0.5, 0.5]], np.float32)
+    r = oracle.verify(c.target, c.draft, c.dtype, c.draft_tokens, c.verify_len, c.T, c.uniforms)
+    assert list(r["accept_len"]) == [0, 1]
+    res = np.cumsum([0.0] + g["residual_normalised"])
+    lo, hi = oracle.draw_cdf(c.target, c.draft, c.dtype, c.verify_len, c.T, 0, 0, [0, 1, 2])
+    np.testing.assert_allclose(lo, res[:3], atol=1e-6)
+    np.testing.assert_allclose(hi, res[1:], atol=1e-6)
+    cp = np.cumsum([0.0] + g["p_target"])
+    lo, hi = oracle.draw_cdf(c.target, c.draft, c.dtype, c.verify_len, c.T, 1, 1, [0, 1, 2])
+    np.testing.assert_allclose(lo, cp[:3], atol=1e-6)
+    np.testing.assert_allclose(hi, cp[1:], atol=1e-6)
+
+
+@pytest.mark.parametrize("name", ["tiny", "mtp_chat"])
+def test_draw_cdf_brackets_the_drawn_token(name):
+    """For every request the lookup gives the drawn token's bin exactly as the
+    draw reported it, u lies inside it, and the bins of all tokens tile [0, 1]
+    in order (hi of v = lo of v + 1, from 0 to 1)."""
+    c = specsynth.make_verify_case(name, B=8, V=3000)
+    r = oracle.verify(c.target, c.draft, c.dtype, c.draft_tokens, c.verify_len, c.T, c.uniforms)
+    for b in range(c.B):
+        n = int(r["accept_len"][b])
+        tok = int(r["tokens"][b, n])
+        lo, hi = oracle.draw_cdf(c.target, c.draft, c.dtype, c.verify_len, c.T, b, n, np.arange(c.V))
+        assert lo[tok] == r["cdf_lo"][b] and hi[tok] == r["cdf_hi"][b]
+        assert lo[tok] <= r["u_draw"][b] < hi[tok]
+        assert lo[0] == 0.0 and abs(hi[-1] - 1.0) < 1e-15
+        assert (hi[:-1] == lo[1:]).all() and (hi >= lo).all()
+
+
 # ------------------------------------------------------------------ statistics
 def _softmax64(z, T):
     """softmax(z / T) in fp64, with T the fp32 temperature widened."""
