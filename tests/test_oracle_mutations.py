@@ -53,6 +53,7 @@ MUTATIONS = {
     "pack_rows_inclusive": ("        target_row[b] = t;\n        draft_row[b] = d;\n        const int ell = verify_len[b];\n        if (ell >= 0 && ell <= gamma) {\n            t += ell + 1;\n            d += ell;\n        }",
                             "        const int ell = verify_len[b];\n        if (ell >= 0 && ell <= gamma) {\n            t += ell + 1;\n            d += ell;\n        }\n        target_row[b] = t;\n        draft_row[b] = d;"),
     "progress_coarse": ("#define PROG_FRAC_BITS 46", "#define PROG_FRAC_BITS 30"),
+    "progress_coarser": ("#define PROG_FRAC_BITS 46", "#define PROG_FRAC_BITS 20"),
     "sts_power_inverted": ("a[i] = prefix[i] * pow((double)conf[(int64_t)i * gamma + k - 1], 1.0 / T);",
                            "a[i] = prefix[i] * pow((double)conf[(int64_t)i * gamma + k - 1], T);"),
 }

@@ -164,3 +164,110 @@ def test_invalid_scheduler_inputs():
     bad[1, 2] = 1.5
     assert oracle.sched_exact(bad, ([0.0], [1.0]))["rc"] == oracle.ERR_CONFIDENCE
     assert oracle.sched_exact(conf, ([0.0], [1.0]), 4)["rc"] == oracle.ERR_SHAPE
+
+
+# ------------------------------------------- the choice, in exact arithmetic
+def _exact_cost(N, cost):
+    """C(N) of a knot table in exact rationals (knots taken as the doubles
+    they are): linear between knots, flat beyond both ends."""
+    from fractions import Fraction
+    kt = [Fraction(float(t)) for t in cost[0]]
+    kc = [Fraction(float(c)) for c in cost[1]]
+    N = Fraction(N)
+    if N <= kt[0]:
+        return kc[0]
+    if N >= kt[-1]:
+        return kc[-1]
+    i = max(j for j in range(len(kt) - 1) if kt[j] <= N)
+    return kc[i] + (N - kt[i]) * (kc[i + 1] - kc[i]) / (kt[i + 1] - kt[i])
+
+
+def _exact_argmax(conf, cost, min_len):
+    """The allocation in [min_len, gamma]^B maximising tau / C(N) exactly:
+    survivals s_{b,k} = prod_{t<k} c_{b,t} (AngelSpec eq. (20)) and progress
+    A_b(l) = sum_{k<=l} s_{b,k} (eq. (21)) as exact rationals of the fp32
+    confidences, tau = sum_b A_b(l_b), N = sum_b (l_b + 1) (eq. (24)).
+    Returns (allocation, relative gap to the best other allocation)."""
+    import itertools
+    from fractions import Fraction
+    B, gamma = conf.shape
+    A = []
+    for b in range(B):
+        s, acc, row = Fraction(1), Fraction(1), [Fraction(1)]
+        for k in range(gamma):
+            s *= Fraction(float(conf[b, k]))
+            acc += s
+            row.append(acc)
+        A.append(row)
+    # every denominator is a power of two: integers over a common one
+    D = max(a.denominator for row in A for a in row)
+    Ai = [[a.numerator * (D // a.denominator) for a in row] for row in A]
+    top = {}   # N -> two largest (tau, allocation)
+    for alloc in itertools.product(range(min_len, gamma + 1), repeat=B):
+        tau = sum(Ai[b][l] for b, l in enumerate(alloc))
+        N = sum(alloc) + B
+        best = top.setdefault(N, [])
+        best.append((tau, alloc))
+        best.sort(key=lambda t: -t[0])
+        del best[2:]
+    objs = []
+    for N, best in top.items():
+        C = _exact_cost(N, cost)
+        for tau, alloc in best:
+            objs.append((Fraction(tau, D) / C, alloc))
+    objs.sort(key=lambda t: -t[0])
+    gap = (objs[0][0] - objs[1][0]) / objs[0][0] if len(objs) > 1 else Fraction(1)
+    return np.array(objs[0][1], np.int32), gap
+
+
+def test_choice_with_survivals_closer_than_2_pow_minus_20():
+    """Two candidates whose survivals differ by 4 fp32 ulps of 0.75 (2.4e-7):
+    the exact order puts request 1 first, and a cost that stops after one
+    extra position must extend request 1, not request 0."""
+    c1 = np.float32(0.75) + np.float32(4 * 2.0 ** -24)
+    conf = np.array([[0.75], [c1]], np.float32)
+    cost = ([0.0, 3.0, 4.0], [1.0, 1.0, 100.0])
+    alloc, gap = _exact_argmax(conf, cost, 0)
+    assert list(alloc) == [0, 1] and gap > 1e-9
+    assert list(oracle.sched_exact(conf, cost, 0)["verify_len"]) == [0, 1]
+
+
+@pytest.mark.parametrize("cost_name", ["affine", "Bprime", "A", "C"])
+@pytest.mark.parametrize("min_len", [0, 1])
+def test_exact_scan_choice_is_the_exact_rational_argmax(cost_name, min_len):
+    """The allocation the oracle's exact scan returns (fixed-point survivals,
+    integer progress sums) is the argmax of tau / C over every allocation in
+    exact rational arithmetic, whenever that argmax leads the next allocation
+    by more than 1e-9 relative.  B <= 4, gamma <= 4; confidences uniform,
+    sigmoid(N(1.5, 1)) as in the scheduled workload, or with near-tied
+    survivals (a few fp32 ulps apart) planted between requests."""
+    rng = np.random.default_rng(70 + min_len + 10 * ["affine", "Bprime", "A", "C"].index(cost_name))
+    kt, kc = COSTS[cost_name]
+    checked = 0
+    trials = 2500
+    for trial in range(trials):
+        B = int(rng.integers(1, 5))
+        gamma = int(rng.integers(max(1, min_len), 5))
+        kind = trial % 3
+        if kind == 0:
+            conf = rng.uniform(0.0, 1.0, (B, gamma)).astype(np.float32)
+        elif kind == 1:
+            z = rng.normal(1.5, 1.0, (B, gamma))
+            conf = (1.0 / (1.0 + np.exp(-z))).astype(np.float32)
+        else:
+            conf = rng.uniform(0.5, 1.0, (B, gamma)).astype(np.float32)
+            for b in range(1, B):
+                ulps = int(rng.integers(-6, 7))
+                conf[b, 0] = np.float32(conf[0, 0] + np.float32(ulps * 2.0 ** -24))
+        s = float(rng.uniform(0.002, 0.2))
+        cost = (np.array(kt) * s, np.array(kc))
+        if cost_name == "affine":
+            cost = ([0.0, 10.0], [1.0, 1.0 + 10.0 * float(rng.uniform(0.01, 2.0))])
+        r = oracle.sched_exact(conf, cost, min_len)
+        assert r["rc"] == 0
+        want, gap = _exact_argmax(conf, cost, min_len)
+        if gap <= 1e-9:
+            continue
+        checked += 1
+        assert np.array_equal(r["verify_len"], want), (trial, conf, r["verify_len"], want, float(gap))
+    assert checked >= 0.9 * trials
