@@ -37,7 +37,7 @@ UNIT = "verified rows/s"
 WORKLOAD = "block_diffusion"
 SEED_OFFSET = 0           # --seed-offset
 COST_READING = "Bprime"   # --cost-table
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "row_stats_block_diffusion.md")
+PROFILE_RECORD = os.path.join(ROOT, "profiles", "row_stats_block_diffusion.json")
 KERNEL_SOURCES = ["speculative_decoding_verification_softmax_gb300/csrc/specv_rowstats.cuh",
                   "speculative_decoding_verification_softmax_gb300/csrc/specv_common.cuh"]
 
@@ -60,17 +60,16 @@ def measured_peak_gbs():
 
 
 def profiled_traffic():
-    """DRAM bytes per launch of the row-statistics kernel from the committed ncu
-    summary, or None if the kernel source changed since the capture."""
+    """DRAM bytes per launch of the row-statistics kernel from the committed
+    ncu record, or None if the kernel source changed since the capture."""
     try:
-        txt = open(PROFILE_SUMMARY).read()
-    except OSError:
+        with open(PROFILE_RECORD) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
         return None
-    m_hash = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", txt)
-    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
-    if not m_hash or not m_tr or m_hash.group(1) != kernel_source_hash():
+    if rec.get("kernel_source_sha") != kernel_source_hash():
         return None
-    return float(m_tr.group(1))
+    return float(rec["traffic_bytes_per_launch"])
 
 
 # ------------------------------------------------------------------ clocks
@@ -226,6 +225,7 @@ def workload_config(case):
 
 
 SCHED_REPLAYS = 200
+PREROLL_STEPS = 20        # untimed calls right before the timed ones
 
 
 def time_schedulers(sv, dev, stream, rank: int):
@@ -312,13 +312,38 @@ def graph_us_per_call(dev, stream, call, n_calls: int = 50, reps: int = 5) -> fl
     return e0.elapsed_time(e1) * 1e3 / (reps * n_calls)
 
 
+def row_stats_ms(sv, dev, stream, call, n: int) -> float:
+    """Mean duration of the row-statistics kernel over n host-launched calls
+    (call(i)), from an event pair recorded on the launching stream right
+    before and after that kernel in each call (spec_profile_events)."""
+    import torch
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, b in pairs:          # create the events before they are timed
+        a.record(stream)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    for i, (a, b) in enumerate(pairs):
+        sv.profile_events(a, b)
+        call(i)
+    torch.cuda.synchronize(dev)
+    sv.profile_events(None, None)
+    return sum(a.elapsed_time(b) for a, b in pairs) / n
+
+
+def roofline_entry(alg_bytes: float, ms: float, launches: int) -> dict:
+    peak, peak_kind = measured_peak_gbs()
+    achieved = alg_bytes / (ms / 1e3) / 1e9
+    return {"kernel": "k_row_stats", "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "algorithmic_bytes_per_launch": alg_bytes, "avg_launch_ms": ms,
+            "launches_timed": launches, "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})"}
+
+
 def time_other_workloads(sv, specsynth, dev, stream, rank: int):
     """Device time per call of the other verification workloads (the small
     ones are latency-bound): 100 calls captured in a CUDA graph and replayed,
     inputs rotated over copies so that each call's working set exceeds twice
     the L2 where that takes at most 32 copies."""
     import torch
-    from tests import _helpers as H
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     out = {}
     for name in ("tiny", "mtp_chat", "greedy"):
@@ -326,7 +351,7 @@ def time_other_workloads(sv, specsynth, dev, stream, rank: int):
         B, gamma, V = case.B, case.gamma, case.V
         bytes_call = case.target.nbytes + (case.draft.nbytes if case.T != 0 else 0)
         n_sets = max(1, min(32, -(-2 * l2 // bytes_call)))
-        sets = [H.to_device(case, dev) for _ in range(n_sets)]
+        sets = [specsynth.to_device(case, dev) for _ in range(n_sets)]
         dt = sv.BF16 if case.dtype == "bf16" else sv.F32
         ws = sv.alloc_verify_workspace(B, gamma, V, dt, dev)
         ot = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
@@ -424,24 +449,26 @@ def time_packed_step(sv, specsynth, case, t, d, x, u, dev, stream, rank: int, st
     torch.cuda.synchronize(dev)
     host_ms = e0.elapsed_time(e1) / steps
     ms = graph_us_per_call(dev, stream, step) / 1e3
-    if sv.read_status(ws) != 0 or sv.read_status(sws) != 0:
-        raise RuntimeError("device status on the packed step")
     rows = int(vl_h.sum())
     logit_bytes = (Kt + Kd) * V * 2
+    k1 = row_stats_ms(sv, dev, stream, step, max(3, min(steps, 200)))
+    if sv.read_status(ws) != 0 or sv.read_status(sws) != 0:
+        raise RuntimeError("device status on the packed step")
     return {"workload": "D-cut budget (ratios 0.25..1, costs = the round-cost table at K_rho), dense packing, "
                         f"verify of the {WORKLOAD} logits packed as [{Kt}, V] target and [{Kd}, V] draft rows",
             "ms_per_step": ms, "verified_rows_per_step": rows, "verified_rows_per_s": rows / (ms / 1e3),
             "packed_logit_bytes": logit_bytes, "logit_gbs": logit_bytes / (ms / 1e3) / 1e9,
-            "timing": f"50 steps in a CUDA graph, 5 replays; packed logits rotated over {n_sets} copies",
+            "timing": f"50 steps in a CUDA graph, 5 replays; packed logits rotated over {n_sets} copies "
+                      f"({n_sets * logit_bytes / 1e6:.0f} MB, L2 {l2 / 1e6:.0f} MB)",
             "host_launched_ms_per_step": host_ms, "host_launched_steps": steps,
-            "kernel_launches_per_step": 2 + sv.kernel_count(B, case.T)}
+            "kernel_launches_per_step": 2 + sv.kernel_count(B, case.T),
+            "roofline": roofline_entry(logit_bytes, k1, max(3, min(steps, 200)))}
 
 
 def run_ours(args):
     import torch
     import specsynth
     import speculative_decoding_verification_softmax_gb300 as sv
-    from tests import _helpers as H
 
     rank, world, local = dist_env()
     if world > 1:
@@ -455,7 +482,7 @@ def run_ours(args):
     case = specsynth.make_verify_case(WORKLOAD, seed_logits=300 + o, seed_noise=301 + o, seed_tokens=302 + o,
                                       seed_uniforms=303 + o)
     B, gamma, V = case.B, case.gamma, case.V
-    t, d, x, vl, u = H.to_device(case, dev)
+    t, d, x, vl, u = specsynth.to_device(case, dev)
     out_t = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
     out_n = torch.empty((B,), dtype=torch.int32, device=dev)
     ws = sv.alloc_verify_workspace(B, gamma, V, sv.BF16, dev)
@@ -478,6 +505,11 @@ def run_ours(args):
     if world > 1:
         torch.distributed.barrier()
     with ClockSampler(local) as clk:
+        # an untimed burst first, so that the timed steps start on a busy GPU
+        # with the host already ahead of it (not from the idle gap of the
+        # clock sampler's start-up)
+        for _ in range(PREROLL_STEPS):
+            step()
         ev0.record(stream)
         for _ in range(args.steps):
             step()
@@ -552,8 +584,19 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     s_host_ms = s0.elapsed_time(s1) / s_steps
     s_ms = graph_us_per_call(dev, stream, sched_step) / 1e3
+    vl_h = vl_s.cpu().numpy()
+    s_rows = int(vl_h.sum())
+    ragged_bytes = int((2 * vl_h + 1).sum()) * V * 2
+
+    def ragged_verify(i=0):     # the verification alone, at the scheduled lengths
+        st_, sd_ = ssets[i % 2]
+        sv.verify(st_, sd_, x, vl_s, case.T, u, out_tokens=out_t, out_accept_len=out_n, workspace=ws)
+
+    rv_ms = graph_us_per_call(dev, stream, ragged_verify) / 1e3
+    n_rag = out_n.cpu().numpy()
+    ragged_resid = int(((n_rag < vl_h) * 2 + (n_rag >= vl_h)).sum()) * V * 2
+    rk1 = row_stats_ms(sv, dev, stream, sched_step, max(3, min(args.steps, 200)))
     del ssets
-    s_rows = int(vl_s.sum().item())
     if sv.read_status(ws) != 0 or sv.read_status(ws_s) != 0:
         raise RuntimeError("device status on the scheduled workload")
     scheduled_step = {"workload": f"schedule (exact scan, cost table {COST_READING}, min_len 1) then verify of the "
@@ -562,8 +605,17 @@ def run_ours(args):
                       "verified_rows_per_s": s_rows / (s_ms / 1e3),
                       "timing": "50 steps in a CUDA graph, 5 replays; logits alternate between two copies",
                       "host_launched_ms_per_step": s_host_ms, "host_launched_steps": s_steps,
-                      "kernel_launches_per_step": 1 + sv.kernel_count(B, case.T)}
+                      "kernel_launches_per_step": 1 + sv.kernel_count(B, case.T),
+                      "logit_bytes_per_step": ragged_bytes,
+                      "verify_only": {"ms_per_call": rv_ms, "bytes_per_call": ragged_bytes + ragged_resid,
+                                      "gbs": (ragged_bytes + ragged_resid) / (rv_ms / 1e3) / 1e9,
+                                      "pct_of_measured_peak": 100.0 * (ragged_bytes + ragged_resid)
+                                      / (rv_ms / 1e3) / 1e9 / measured_peak_gbs()[0],
+                                      "timing": "50 calls in a CUDA graph, 5 replays; logits alternate "
+                                                "between two copies"},
+                      "roofline": roofline_entry(ragged_bytes, rk1, max(3, min(args.steps, 200)))}
     sched = time_schedulers(sv, dev, stream, rank)
+    scheduled_step["scheduler_share"] = sched["modes"]["exact"]["us_per_call"] / 1e3 / s_ms
     packed_step = time_packed_step(sv, specsynth, case, t, d, x, u, dev, stream, rank, s_steps)
     others = time_other_workloads(sv, specsynth, dev, stream, rank)
 
@@ -705,10 +757,9 @@ def run_profile_case(args):
     import torch
     import specsynth
     import speculative_decoding_verification_softmax_gb300 as sv
-    from tests import _helpers as H
     sv.build()
     case = specsynth.make_verify_case(WORKLOAD, B=args.profile_batch)
-    t, d, x, vl, u = H.to_device(case)
+    t, d, x, vl, u = specsynth.to_device(case)
     ws = sv.alloc_verify_workspace(case.B, case.gamma, case.V, sv.BF16)
     for _ in range(args.warmup + args.steps):
         sv.verify(t, d, x, vl, case.T, u, workspace=ws)

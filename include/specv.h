@@ -280,8 +280,10 @@ int spec_sts_fit(const float* confidence, const int32_t* accept_len, int n, int 
  *     spec_verify_workspace_bytes(B, gamma, V, dt) exceeds
  *     SPEC_STATIC_WORKSPACE_BYTES (e.g. B=64, gamma=16, V=131072 bf16 needs
  *     about 1.1 MiB; B=256, gamma=16, V=131072 about 4.3 MiB).
- *   - The first call on a device looks up the array's device address with that
- *     device current; make that first call before any stream capture.
+ *   - Every call looks up the array's device address on the current device
+ *     (so an address never outlives a cudaDeviceReset).  The first lookup on a
+ *     device may load the library's device code; make that first call before
+ *     any stream capture.
  *   - Every call on a device uses the same array and leaves its contents
  *     behind.  Nothing in it needs to start at zero.  Calls that can overlap
  *     on the GPU (different streams without ordering, or several host threads)

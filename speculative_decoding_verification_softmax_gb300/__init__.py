@@ -187,6 +187,39 @@ def _dtype_code(t) -> int:
     raise TypeError(f"logits must be bfloat16 or float32, got {t.dtype}")
 
 
+def _check_tensor(name, t, dtype, shape, required=True):
+    """A contiguous tensor of `dtype` and `shape` on the current CUDA device
+    (the device whose current stream the call uses), or None if allowed."""
+    torch = _torch()
+    if t is None:
+        if required:
+            raise ValueError(f"{name} is required")
+        return
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device}, but the current device is cuda:{torch.cuda.current_device()}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _check_verify_inputs(B, gamma, V, ldtype, draft_logits, draft_shape, draft_tokens, verify_len, temperature,
+                         uniforms, out_tokens, out_accept_len):
+    """Shapes, dtypes and devices of every tensor a verify call reads or writes
+    (the library reads them with the sizes it is given, so a mismatch here
+    would be an out-of-bounds access on the device)."""
+    torch = _torch()
+    greedy = float(temperature) == 0.0
+    _check_tensor("draft_logits", draft_logits, ldtype, draft_shape, required=not greedy and gamma > 0)
+    _check_tensor("draft_tokens", draft_tokens, torch.int32, (B, gamma), required=gamma > 0)
+    _check_tensor("verify_len", verify_len, torch.int32, (B,), required=False)
+    _check_tensor("uniforms", uniforms, torch.float32, (B, gamma + 2), required=not greedy)
+    _check_tensor("out_tokens", out_tokens, torch.int32, (B, gamma + 1), required=False)
+    _check_tensor("out_accept_len", out_accept_len, torch.int32, (B,), required=False)
+
+
 def verify_workspace_bytes(B: int, gamma: int, V: int, dtype_code: int) -> int:
     return int(lib().spec_verify_workspace_bytes(B, gamma, V, dtype_code))
 
@@ -213,12 +246,11 @@ def verify(target_logits, draft_logits, draft_tokens, verify_len, temperature: f
     gamma = G1 - 1
     dt = _dtype_code(target_logits)
     dev = target_logits.device
-    for name, t in (("target_logits", target_logits), ("draft_logits", draft_logits),
-                    ("draft_tokens", draft_tokens), ("verify_len", verify_len), ("uniforms", uniforms)):
-        if t is not None and (not t.is_cuda or not t.is_contiguous()):
-            raise ValueError(f"{name} must be a contiguous CUDA tensor")
-    if draft_logits is not None and draft_logits.dtype != target_logits.dtype:
-        raise TypeError("draft_logits must have the dtype of target_logits")
+    _check_tensor("target_logits", target_logits, target_logits.dtype, (B, G1, V))
+    _check_verify_inputs(B, gamma, V, target_logits.dtype, draft_logits, (B, gamma, V), draft_tokens, verify_len,
+                         temperature, uniforms, out_tokens, out_accept_len)
+    if workspace is not None:
+        _check_tensor("workspace", workspace, torch.uint8, (workspace.numel(),))
     if out_tokens is None:
         out_tokens = torch.empty((B, G1), dtype=torch.int32, device=dev)
     if out_accept_len is None:
@@ -245,10 +277,9 @@ def verify_static(target_logits, draft_logits, draft_tokens, verify_len, tempera
     gamma = G1 - 1
     dt = _dtype_code(target_logits)
     dev = target_logits.device
-    for name, t in (("target_logits", target_logits), ("draft_logits", draft_logits),
-                    ("draft_tokens", draft_tokens), ("verify_len", verify_len), ("uniforms", uniforms)):
-        if t is not None and (not t.is_cuda or not t.is_contiguous()):
-            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    _check_tensor("target_logits", target_logits, target_logits.dtype, (B, G1, V))
+    _check_verify_inputs(B, gamma, V, target_logits.dtype, draft_logits, (B, gamma, V), draft_tokens, verify_len,
+                         temperature, uniforms, out_tokens, out_accept_len)
     if out_tokens is None:
         out_tokens = torch.empty((B, G1), dtype=torch.int32, device=dev)
     if out_accept_len is None:
@@ -274,13 +305,13 @@ def verify_packed(target_logits, draft_logits, target_row, draft_row, draft_toke
     Kd = draft_logits.shape[0] if draft_logits is not None else 0
     dt = _dtype_code(target_logits)
     dev = target_logits.device
-    for name, t in (("target_logits", target_logits), ("draft_logits", draft_logits), ("target_row", target_row),
-                    ("draft_row", draft_row), ("draft_tokens", draft_tokens), ("verify_len", verify_len),
-                    ("uniforms", uniforms)):
-        if t is not None and (not t.is_cuda or not t.is_contiguous()):
-            raise ValueError(f"{name} must be a contiguous CUDA tensor")
-    if draft_logits is not None and (draft_logits.dtype != target_logits.dtype or draft_logits.shape[1] != V):
-        raise TypeError("draft_logits must have the dtype and vocabulary of target_logits")
+    _check_tensor("target_logits", target_logits, target_logits.dtype, (Kt, V))
+    _check_verify_inputs(B, gamma, V, target_logits.dtype, draft_logits, (Kd, V), draft_tokens, verify_len,
+                         temperature, uniforms, out_tokens, out_accept_len)
+    _check_tensor("target_row", target_row, torch.int32, (B,))
+    _check_tensor("draft_row", draft_row, torch.int32, (B,), required=float(temperature) != 0.0 and gamma > 0)
+    if workspace is not None:
+        _check_tensor("workspace", workspace, torch.uint8, (workspace.numel(),))
     if out_tokens is None:
         out_tokens = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
     if out_accept_len is None:
@@ -303,6 +334,9 @@ def pack_rows(verify_len, gamma: int, *, target_row=None, draft_row=None, totals
     torch = _torch()
     B = verify_len.shape[0]
     dev = verify_len.device
+    _check_tensor("verify_len", verify_len, torch.int32, (B,))
+    for name, t, shp in (("target_row", target_row, (B,)), ("draft_row", draft_row, (B,)), ("totals", totals, (2,))):
+        _check_tensor(name, t, torch.int32, shp, required=False)
     if target_row is None:
         target_row = torch.empty((B,), dtype=torch.int32, device=dev)
     if draft_row is None:
@@ -346,8 +380,8 @@ def schedule(confidence, cost, min_len: int = 0, mode: int = SCHED_EXACT, *, sts
     temperatures or None.  Returns (out_verify_len [B] int32, workspace)."""
     torch = _torch()
     B, gamma = confidence.shape
-    if not confidence.is_cuda or not confidence.is_contiguous() or confidence.dtype != torch.float32:
-        raise ValueError("confidence must be a contiguous float32 CUDA tensor")
+    _check_tensor("confidence", confidence, torch.float32, (B, gamma))
+    _check_tensor("out_verify_len", out_verify_len, torch.int32, (B,), required=False)
     table = cost if isinstance(cost, CostTable) else CostTable.from_knots(*cost)
     if out_verify_len is None:
         out_verify_len = torch.empty((B,), dtype=torch.int32, device=confidence.device)
@@ -368,6 +402,8 @@ def schedule_static(confidence, threshold: float, max_len: int, min_len: int = 0
     clamped to [min_len, max_len] (threshold <= 0: fixed length max_len)."""
     torch = _torch()
     B, gamma = confidence.shape
+    _check_tensor("confidence", confidence, torch.float32, (B, gamma), required=threshold > 0)
+    _check_tensor("out_verify_len", out_verify_len, torch.int32, (B,), required=False)
     if out_verify_len is None:
         out_verify_len = torch.empty((B,), dtype=torch.int32, device=confidence.device)
     if workspace is None:

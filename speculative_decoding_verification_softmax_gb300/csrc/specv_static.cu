@@ -12,8 +12,6 @@
 // library is loaded on a GPU and held until the process exits.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "specv_common.cuh"
 
 namespace {
@@ -23,21 +21,16 @@ namespace {
 // address comes from cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_static_workspace[SPEC_STATIC_WORKSPACE_BYTES];
 
-std::mutex g_static_mu;
-void* g_static_ptr[64];  // device address of g_static_workspace, per device
-
-// Looks up (once per device, with that device current) the device address of
-// the static scratch array.
+// The device address of the static scratch array on the current device.  It
+// is looked up on every call (a host-side table lookup once the module is
+// loaded), so that an address never outlives the context it belongs to: after
+// cudaDeviceReset the module is loaded again and the array may move.  The
+// first lookup on a device may load the module, which is why the first call
+// belongs before any stream capture.
 int static_workspace(void** out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPEC_ERR_CUDA;
-    std::lock_guard<std::mutex> lk(g_static_mu);
-    if (!g_static_ptr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || !p) return SPEC_ERR_CUDA;
-        g_static_ptr[dev] = p;
-    }
-    *out = g_static_ptr[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || !p) return SPEC_ERR_CUDA;
+    *out = p;
     return SPEC_OK;
 }
 

@@ -27,16 +27,36 @@ def test_clock_summary_parses_samples():
 
 
 def test_traffic_is_reported_only_for_the_profiled_source(tmp_path, monkeypatch):
-    good = tmp_path / "good.md"
-    good.write_text(f"kernel_source_sha: {bench.kernel_source_hash()}\ntraffic_bytes_per_launch: 123456\n")
-    stale = tmp_path / "stale.md"
-    stale.write_text("kernel_source_sha: 0000000000000000\ntraffic_bytes_per_launch: 123456\n")
-    monkeypatch.setattr(bench, "PROFILE_SUMMARY", str(good))
+    good = tmp_path / "good.json"
+    good.write_text(json.dumps({"kernel_source_sha": bench.kernel_source_hash(),
+                                "traffic_bytes_per_launch": 123456}))
+    stale = tmp_path / "stale.json"
+    stale.write_text(json.dumps({"kernel_source_sha": "0000000000000000", "traffic_bytes_per_launch": 123456}))
+    bad = tmp_path / "bad.json"
+    bad.write_text("kernel_source_sha: not json")
+    monkeypatch.setattr(bench, "PROFILE_RECORD", str(good))
     assert bench.profiled_traffic() == 123456.0
-    monkeypatch.setattr(bench, "PROFILE_SUMMARY", str(stale))
-    assert bench.profiled_traffic() is None
-    monkeypatch.setattr(bench, "PROFILE_SUMMARY", str(tmp_path / "missing.md"))
-    assert bench.profiled_traffic() is None
+    for f in (stale, bad, tmp_path / "missing.json"):
+        monkeypatch.setattr(bench, "PROFILE_RECORD", str(f))
+        assert bench.profiled_traffic() is None
+
+
+def test_product_arm_does_not_load_the_oracle():
+    """Only the CPU-baseline and reference legs may load the oracle: bench.py
+    itself imports neither it nor the test helpers at module level, and the
+    product arm's functions take their inputs from the generator module."""
+    import ast
+    src = open(bench.__file__).read()
+    tree = ast.parse(src)
+    top = [n for n in tree.body if isinstance(n, (ast.Import, ast.ImportFrom))]
+    names = {a.name for n in top for a in n.names} | {getattr(n, "module", None) for n in top}
+    assert "oracle" not in names and "tests" not in names
+    assert "_helpers" not in src
+    for fn in tree.body:
+        if isinstance(fn, ast.FunctionDef) and fn.name not in ("time_oracle",):
+            for n in ast.walk(fn):
+                if isinstance(n, ast.Import):
+                    assert all(a.name != "oracle" for a in n.names), fn.name
 
 
 def test_kernel_source_hash_follows_the_sources(tmp_path, monkeypatch):

@@ -238,3 +238,33 @@ def test_repeated_calls_are_deterministic():
     b = H.gpu_verify(case)
     assert (a["tokens"] == b["tokens"]).all() and (a["accept_len"] == b["accept_len"]).all()
     assert np.array_equal(a["px"], b["px"], equal_nan=True)
+
+
+def test_wrappers_reject_mismatched_inputs():
+    """The binding checks dtype, shape and device of every tensor against
+    (B, gamma, V) before calling the library, for spec_verify and
+    spec_verify_static alike: a draft in another dtype or a short token,
+    length or uniform array would otherwise be read out of bounds."""
+    import torch
+    import speculative_decoding_verification_softmax_gb300 as sv
+    case = specsynth.make_verify_case("mtp_chat", B=4, V=1000)
+    t, d, x, vl, u = H.to_device(case)
+    bad = {
+        "draft dtype": dict(d=d.float()),
+        "draft shape": dict(d=d[:, :-1].contiguous()),
+        "tokens dtype": dict(x=x.long()),
+        "tokens shape": dict(x=x[:-1].contiguous()),
+        "verify_len shape": dict(vl=vl[:-1].contiguous()),
+        "uniforms shape": dict(u=u[:, :-1].contiguous()),
+        "uniforms missing": dict(u=None),
+        "tokens on the host": dict(x=x.cpu()),
+        "draft not contiguous": dict(d=d.transpose(0, 1).contiguous().transpose(0, 1)),
+    }
+    for fn in (lambda a: sv.verify(a["t"], a["d"], a["x"], a["vl"], case.T, a["u"]),
+               lambda a: sv.verify_static(a["t"], a["d"], a["x"], a["vl"], case.T, a["u"])):
+        for what, over in bad.items():
+            args = {**dict(t=t, d=d, x=x, vl=vl, u=u), **over}
+            with pytest.raises((TypeError, ValueError)):
+                fn(args)
+        fn(dict(t=t, d=d, x=x, vl=vl, u=u))   # the well-formed call still runs
+    torch.cuda.synchronize()
