@@ -38,10 +38,12 @@
  *   - A negative return value is an error detected on the host: nothing was
  *     launched and no output was written.  Errors found in device data (a bad
  *     token id, a NaN row, ...) mark the affected request (out_accept_len = -1,
- *     its tokens -1) and set a sticky status word in the workspace, read with
- *     spec_read_status.
- *   - Every device wait in the kernels is bounded; on expiry a kernel records
- *     SPEC_ERR_TIMEOUT in the status word and returns.
+ *     its tokens -1) and set a status word in the workspace, read with
+ *     spec_read_status.  For spec_verify the word holds the status of the most
+ *     recent call on that workspace (each call resets it); for the schedulers
+ *     it is sticky until read.
+ *   - Every device wait in the kernels is bounded; on expiry the call reports
+ *     SPEC_ERR_TIMEOUT in the status word and the kernel returns.
  */
 #ifndef SPECV_H
 #define SPECV_H
@@ -109,9 +111,11 @@ size_t spec_verify_workspace_bytes(int B, int gamma, int V, spec_dtype dt);
  *   out_accept_len [B] int32: n, the number of accepted drafts (-1 if the
  *                  request's inputs were invalid).
  *   workspace      device scratch of at least spec_verify_workspace_bytes(),
- *                  16-byte aligned; holds the sticky status word.  Its contents
- *                  need no initialisation.  Two calls sharing one workspace
- *                  must be ordered on the same stream.
+ *                  16-byte aligned; holds the status word of the most recent
+ *                  call (reset by each call, read and cleared by
+ *                  spec_read_status).  Its contents need no initialisation.
+ *                  Two calls sharing one workspace must be ordered on the same
+ *                  stream.
  * Draws use the inverse CDF: the token is the smallest v whose running sum of
  * weights exceeds u * (sum of weights).  Returns SPEC_OK or a host-detected
  * error (nothing launched).  B == 0 returns SPEC_OK without launching.
@@ -311,10 +315,24 @@ int spec_verify_static(const void* target_logits, const void* draft_logits, spec
 int spec_selftest_wait(long long limit_ns, int32_t* status, unsigned long long* elapsed_ns,
                        spec_stream_t stream);
 
+/*
+ * Test hook of the streaming kernel's timeout path (off by default).  While
+ * `on` is nonzero, later spec_verify calls (made from any thread) treat the
+ * first copy wait of every warp of the streaming kernel as expired, without
+ * waiting for it.  The warps then let their copies in flight land (each wait
+ * bounded as usual) and stop; the call marks every request invalid
+ * (out_accept_len = -1) and its status word reads SPEC_ERR_TIMEOUT.  No copy
+ * is lost and nothing hangs; it exercises the path that a bulk copy which
+ * never completes would take.  Returns SPEC_OK.
+ */
+int spec_selftest_expire_first_wait(int on);
+
 /* ------------------------------------------------------------------ status */
 
-/* Synchronises `stream`, reads the sticky device status word of `workspace`
- * into *status and clears it.  Returns SPEC_OK or SPEC_ERR_CUDA. */
+/* Synchronises `stream`, reads the device status word of `workspace` into
+ * *status and clears it: for a verification workspace the status of the most
+ * recent call on it, for a scheduler workspace the first error since the last
+ * read.  Returns SPEC_OK or SPEC_ERR_CUDA. */
 int spec_read_status(void* workspace, spec_stream_t stream, int* status);
 
 /* A static English description of a status code. */

@@ -35,7 +35,7 @@ EXPORTED = ["spec_verify_workspace_bytes", "spec_verify", "spec_verify_stats",
             "spec_schedule_workspace_bytes", "spec_schedule", "spec_read_status",
             "spec_status_string", "spec_profile_events", "spec_verify_kernel_count",
             "spec_verify_static", "spec_schedule_static", "spec_sts_fit", "spec_verify_packed",
-            "spec_pack_rows", "spec_selftest_wait"]
+            "spec_pack_rows", "spec_selftest_wait", "spec_selftest_expire_first_wait"]
 STATIC_WORKSPACE_BYTES = 8 << 20
 
 
@@ -129,6 +129,8 @@ def lib():
                 L.spec_pack_rows.restype = i32
                 L.spec_selftest_wait.argtypes = [ctypes.c_longlong, vp, vp, vp]
                 L.spec_selftest_wait.restype = i32
+                L.spec_selftest_expire_first_wait.argtypes = [i32]
+                L.spec_selftest_expire_first_wait.restype = i32
                 _lib = L
     return _lib
 
@@ -225,6 +227,7 @@ def verify_workspace_bytes(B: int, gamma: int, V: int, dtype_code: int) -> int:
 
 
 def alloc_verify_workspace(B: int, gamma: int, V: int, dtype_code: int, device=None):
+    """A verification workspace (its contents need no initialisation)."""
     torch = _torch()
     n = verify_workspace_bytes(B, gamma, V, dtype_code)
     if n == 0:
@@ -440,6 +443,12 @@ def selftest_wait(limit_ns: int = 1_000_000, stream=None):
     _check(lib().spec_selftest_wait(int(limit_ns), _ptr(st), _ptr(el), _stream_handle(stream)), "spec_selftest_wait")
     torch.cuda.synchronize()
     return tuple(int(v) for v in st.cpu()), tuple(int(v) for v in el.cpu())
+
+
+def selftest_expire_first_wait(on: bool) -> None:
+    """Test hook: while on, the first copy wait of every streaming warp in later
+    verify calls counts as expired (the timeout path; see include/specv.h)."""
+    _check(lib().spec_selftest_expire_first_wait(1 if on else 0), "spec_selftest_expire_first_wait")
 
 
 def read_status(workspace, stream=None) -> int:

@@ -19,6 +19,9 @@ constexpr int kStatsWarps = 20;
 constexpr int kStages = 2;
 // Bound on any device wait (nanoseconds of %globaltimer).
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+// Largest grid of the streaming kernel (one word per CTA in the workspace,
+// read by the finish kernel's first warp as two 16-byte vectors per lane).
+constexpr int kMaxStatsGrid = 256;
 
 // ----------------------------------------------------------- workspace
 // Per-request state written by the accept kernel, read by the draw kernel.
@@ -100,7 +103,7 @@ struct Layout {
     int R;        // B * (2*gamma + 1) potential rows
     int nch;      // chunks per row
     int CH;       // elements per chunk
-    size_t hdr, partial, req, pq, mass, rchunk, total;
+    size_t hdr, ctaw, partial, req, pq, mass, rchunk, total;
 
     __host__ __device__ static size_t up(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -110,6 +113,7 @@ struct Layout {
         nch = (int)(((long long)V + CH - 1) / CH);
         size_t o = 0;
         hdr = o;      o = up(o + 256);
+        ctaw = o;     o = up(o + sizeof(int) * (size_t)kMaxStatsGrid);
         partial = o;  o = up(o + sizeof(float2) * (size_t)R * (size_t)nch);
         req = o;      o = up(o + sizeof(ReqState) * (size_t)B);
         pq = o;       o = up(o + 2 * sizeof(float) * (size_t)B * (size_t)(gamma > 0 ? gamma : 1));
@@ -119,7 +123,11 @@ struct Layout {
     }
 };
 
-// Header words (int32) at the start of the workspace.
+// Header words (int32) at the start of the workspace: the status of the most
+// recent call (reset by its streaming kernel, set by its finish kernel, read
+// and cleared by spec_read_status) and its event bits.  Timeouts of the
+// streaming kernel go to one word per CTA (the `ctaw` section), written by
+// every CTA of every call, so no CTA's reset can race with another's error.
 constexpr int kHdrStatus = 0;
 constexpr int kHdrEvents = 2;
 

@@ -54,6 +54,7 @@ struct StatsArgs {
     float c_hi, c_lo;
     char* ws;
     RowMap rm;
+    int expire_first;  // test hook: each warp's first wait counts as expired (0 in normal use)
 };
 
 // Rows a request needs: target 0..ell and (T > 0) draft 0..ell-1; 0 when
@@ -283,18 +284,20 @@ __global__ void __launch_bounds__(kStatsThreads, 1) k_row_stats(StatsArgs a, Lay
     int* table = prefix + (SPEC_MAX_BATCH + 1);
     int* hdr = (int*)(a.ws + L.hdr);
     float2* partial = (float2*)(a.ws + L.partial);
+    __shared__ int s_exited, s_failed;  // warps done / any wait expired (this CTA)
 
     if (lane == 0) {
         for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
         fence_mbar_init();
     }
+    if (tid == 0) s_exited = s_failed = 0;  // published by the barriers in block_row_prefix
     // launched as a programmatic dependent of the preceding kernel in the
     // stream: nothing in global memory is read or written before its results
     // are complete and visible
     pdl_wait();
-    if (blockIdx.x == 0 && tid == 0) {  // per-call reset of the status words
-        hdr[kHdrStatus] = 0;
-        hdr[kHdrEvents] = 0;
+    if (blockIdx.x == 0 && tid == 0) {  // per-call reset of the status words (only the
+        hdr[kHdrStatus] = 0;             // finish kernel, which runs after every CTA of
+        hdr[kHdrEvents] = 0;             // this grid, sets them)
     }
     block_row_prefix<GREEDY, PACKED>(a.verify_len, a.rm, a.B, a.gamma, prefix);
     pdl_trigger();
@@ -342,6 +345,19 @@ __global__ void __launch_bounds__(kStatsThreads, 1) k_row_stats(StatsArgs a, Lay
         }
         const int gd = g - T1, b = gd / a.gamma;
         return a.draft + draft_row(a.rm, b, gd - b * a.gamma, a.gamma) * a.V * ES;
+    };
+
+    // Every warp ends here: the last warp of the CTA to leave writes the CTA's
+    // word (SPEC_ERR_TIMEOUT if any of its waits expired, else SPEC_OK).
+    auto warp_exit = [&](bool failed) {
+        if (lane == 0) {
+            if (failed) atomicOr(&s_failed, 1);
+            __threadfence_block();
+            if (atomicAdd(&s_exited, 1) == kStatsWarps - 1) {
+                __threadfence_block();
+                ((int*)(a.ws + L.ctaw))[blockIdx.x] = atomicOr(&s_failed, 0) ? SPEC_ERR_TIMEOUT : SPEC_OK;
+            }
+        }
     };
 
     Cursor ic{gw / nch, gw - (gw / nch) * nch, 0};  // issue cursor
@@ -393,10 +409,14 @@ __global__ void __launch_bounds__(kStatsThreads, 1) k_row_stats(StatsArgs a, Lay
         __syncthreads();
         table_ready = true;
     }
-    if (!has_items) return;
+    if (!has_items) {
+        warp_exit(false);
+        return;
+    }
     __syncwarp();
 
     int s = 0;
+    bool failed = false;
 #pragma unroll 1
     for (long long done = 0; done < count; ++done) {
         int g, c, nvec, base, si = -1;
@@ -416,12 +436,12 @@ __global__ void __launch_bounds__(kStatsThreads, 1) k_row_stats(StatsArgs a, Lay
             if (si >= 0) sv = load_logit<ES>(d.sp.rowp, si);
         }
         if (pending & (1u << s)) {
-            if (!mbar_wait_bounded(&bars[s], (phase >> s) & 1u)) {
-                // record the failure and let this warp's copies in flight land
-                if (lane == 0) set_status(&hdr[kHdrStatus], SPEC_ERR_TIMEOUT);
-                for (int k = 0; k < kStages; ++k)
-                    if (k != s && (pending & (1u << k))) mbar_wait_bounded(&bars[k], (phase >> k) & 1u);
-                return;
+            // every lane waits (each observes the copy's completion); the warp
+            // goes on only if all of them saw it
+            const bool ok = !(a.expire_first && done == 0) && mbar_wait_bounded(&bars[s], (phase >> s) & 1u);
+            if (!__all_sync(0xffffffffu, ok)) {
+                failed = true;
+                break;
             }
             phase ^= 1u << s;
             pending &= ~(1u << s);
@@ -437,6 +457,15 @@ __global__ void __launch_bounds__(kStatsThreads, 1) k_row_stats(StatsArgs a, Lay
         advance(cc);
         s = (s + 1 == kStages) ? 0 : s + 1;
     }
+    if (failed) {
+        // a wait expired: let every copy this warp still has in flight land,
+        // the expired one included (each again bounded), so that no copy
+        // completes into the shared memory of an exited CTA
+        for (int k = 0; k < kStages; ++k)
+            if (pending & (1u << k)) mbar_wait_bounded(&bars[k], (phase >> k) & 1u);
+        __syncwarp();
+    }
+    warp_exit(failed);
 }
 
 }  // namespace specv

@@ -461,6 +461,7 @@ struct FinishArgs {
     float c_hi, c_lo;
     char* ws;
     RowMap rm;
+    int stats_grid;  // CTAs of the streaming kernel (one timeout word each)
 };
 
 struct RowStatS {
@@ -510,6 +511,7 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
     __shared__ float s_ctot[kChunkSmem];
     __shared__ float s_rsum[kRoundSmem][8];
     __shared__ ReqState s_job;
+    __shared__ int s_call_status;
     int* hdr = (int*)(a.ws + L.hdr);
     const float2* partial = (const float2*)(a.ws + L.partial);
     const int G1 = a.gamma + 1, T1 = a.B * G1;
@@ -546,9 +548,25 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
             if (!__all_sync(0xffffffffu, uok)) st = SPEC_ERR_UNIFORM;
         }
     }
-    pdl_wait();  // the streaming kernel's partials and status word
+    pdl_wait();  // the streaming kernel's partials and timeout words
     pdl_trigger();
-    const bool timed_out = warp == 0 && hdr[kHdrStatus] == SPEC_ERR_TIMEOUT;
+    // Whether a streaming CTA's wait expired, taken by the cluster's last warp
+    // (idle in the merges unless the rows outnumber the warps) and sent to
+    // every CTA of the cluster.
+    if (gw == nw - 1) {
+        const int4* w4 = (const int4*)(a.ws + L.ctaw);
+        const int4 v0 = 4 * lane < a.stats_grid ? w4[lane] : make_int4(0, 0, 0, 0);
+        const int4 v1 = 4 * (lane + 32) < a.stats_grid ? w4[lane + 32] : make_int4(0, 0, 0, 0);
+        const int w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        bool late = false;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int i = (k < 4 ? 4 * lane : 4 * (lane + 32)) + (k & 3);
+            late |= i < a.stats_grid && w[k] != SPEC_OK;
+        }
+        const int v = __any_sync(0xffffffffu, late) ? SPEC_ERR_TIMEOUT : SPEC_OK;
+        if (lane < cs) *cluster.map_shared_rank(&s_call_status, lane) = v;
+    }
 
     // 2. row merges: target rows 0..ell, then draft rows 0..ell-1
     const int nrows = rows_ok ? (GREEDY ? ell + 1 : 2 * ell + 1) : 0;
@@ -563,7 +581,7 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
 
     // 3. accept decision (identical in every CTA)
     if (warp == 0) {
-        if (timed_out) st = SPEC_ERR_TIMEOUT;
+        if (s_call_status != SPEC_OK) st = s_call_status;
         if (st == SPEC_OK) {
             bool bad = false;
             for (int r = lane; r < nrows; r += 32) bad |= s_row[r].S.hi != s_row[r].S.hi;
@@ -897,6 +915,8 @@ namespace {
 // profiling hook (spec_profile_events): atomics, so that setting it from one
 // thread while another launches is not a data race
 std::atomic<cudaEvent_t> g_ev_before{nullptr}, g_ev_after{nullptr};
+// test hook (spec_selftest_expire_first_wait)
+std::atomic<int> g_expire_first{0};
 
 struct DeviceInfo {
     int sms = 0;
@@ -944,7 +964,7 @@ template <int ES, bool GREEDY>
 int launch_chain(const StatsArgs& sa, const FinishArgs& fa, const Layout& L, int sms, bool aligned_rows,
                  cudaStream_t st) {
     const long long max_items = (long long)L.R * L.nch;
-    const int grid = (int)std::min<long long>(sms, (max_items + kStatsWarps - 1) / kStatsWarps);
+    const int grid = (int)std::min<long long>(std::min(sms, kMaxStatsGrid), (max_items + kStatsWarps - 1) / kStatsWarps);
     const bool packed = sa.rm.trow != nullptr;
     const cudaEvent_t ev_before = g_ev_before.load(std::memory_order_relaxed);
     const cudaEvent_t ev_after = g_ev_after.load(std::memory_order_relaxed);
@@ -971,6 +991,8 @@ int launch_chain(const StatsArgs& sa, const FinishArgs& fa, const Layout& L, int
         if (ke != cudaSuccess) return SPEC_ERR_CUDA;
     }
     if (ev_after) cudaEventRecord(ev_after, st);
+    FinishArgs fa2 = fa;
+    fa2.stats_grid = grid;
     // one cluster per request; it may be scheduled while the streaming kernel
     // finishes and waits for its results with griddepcontrol.wait
     const int cs = finish_cluster_size(sa.B, sa.gamma, L.nch, GREEDY, sms);
@@ -990,8 +1012,8 @@ int launch_chain(const StatsArgs& sa, const FinishArgs& fa, const Layout& L, int
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     cudaError_t e;
-    if (GREEDY || !split) e = cudaLaunchKernelEx(&cfg, k_finish<ES, GREEDY, false>, fa, L);
-    else e = cudaLaunchKernelEx(&cfg, k_finish<ES, GREEDY, !GREEDY>, fa, L);
+    if (GREEDY || !split) e = cudaLaunchKernelEx(&cfg, k_finish<ES, GREEDY, false>, fa2, L);
+    else e = cudaLaunchKernelEx(&cfg, k_finish<ES, GREEDY, !GREEDY>, fa2, L);
     if (e != cudaSuccess) return SPEC_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
@@ -1031,9 +1053,9 @@ int verify_impl(const void* target_logits, const void* draft_logits, const RowMa
     const char* t = (const char*)target_logits;
     const char* d = (const char*)draft_logits;
     char* ws = (char*)workspace;
-    StatsArgs sa{t, d, verify_len, B, gamma, V, c_hi, c_lo, ws, rm};
-    FinishArgs fa{t,     d,     draft_tokens, verify_len, uniforms, out_tokens, out_accept_len, B, gamma, V,
-                  c_hi, c_lo, ws,           rm};
+    StatsArgs sa{t, d, verify_len, B, gamma, V, c_hi, c_lo, ws, rm, g_expire_first.load(std::memory_order_relaxed)};
+    FinishArgs fa{t,    d,    draft_tokens, verify_len, uniforms, out_tokens, out_accept_len, B, gamma, V,
+                  c_hi, c_lo, ws,           rm,         0};
     cudaStream_t st = (cudaStream_t)stream;
     // every row starts on a 16-byte boundary: whole-chunk copies
     const bool al = aligned(target_logits, 16) && (greedy || gamma == 0 || !draft_logits || aligned(draft_logits, 16)) &&
@@ -1110,6 +1132,11 @@ int spec_verify_stats(const void* workspace, size_t workspace_bytes, int B, int 
 int spec_profile_events(void* before_row_stats, void* after_row_stats) {
     g_ev_before.store((cudaEvent_t)before_row_stats, std::memory_order_relaxed);
     g_ev_after.store((cudaEvent_t)after_row_stats, std::memory_order_relaxed);
+    return SPEC_OK;
+}
+
+int spec_selftest_expire_first_wait(int on) {
+    g_expire_first.store(on ? 1 : 0, std::memory_order_relaxed);
     return SPEC_OK;
 }
 

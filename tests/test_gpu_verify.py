@@ -268,3 +268,4 @@ def test_wrappers_reject_mismatched_inputs():
                 fn(args)
         fn(dict(t=t, d=d, x=x, vl=vl, u=u))   # the well-formed call still runs
     torch.cuda.synchronize()
+

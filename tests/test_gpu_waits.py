@@ -32,3 +32,31 @@ def test_context_usable_after_a_timeout(sv):
     P = H.compare(o, g["tokens"], g["accept_len"], g["px"], g["qx"], g["mass"], g["status"])
     assert g["device_status"] == 0
     H.assert_parity(P)
+
+
+@pytest.mark.parametrize("name,T", [("mtp_chat", None), ("greedy", 0.0)])
+def test_streaming_kernel_timeout_path(sv, name, T):
+    """The real streaming kernel's timeout path: with the test hook on, the
+    first copy wait of every warp counts as expired; the warps let their
+    copies land and stop, the call reports SPEC_ERR_TIMEOUT and marks every
+    request invalid.  The next call on the same workspace, hook off, matches
+    the oracle."""
+    import numpy as np
+    case = specsynth.make_verify_case(name, B=8, V=20000)
+    T = case.T if T is None else T
+    t, d, x, vl, u = specsynth.to_device(case)
+    uu = u if T != 0 else None
+    sv.selftest_expire_first_wait(True)
+    try:
+        tok, n, ws = sv.verify(t, d, x, vl, T, uu)
+        st = sv.read_status(ws)
+    finally:
+        sv.selftest_expire_first_wait(False)
+    assert st == sv.ERR_TIMEOUT
+    assert (n.cpu().numpy() == -1).all() and (tok.cpu().numpy() == -1).all()
+    tok, n, ws = sv.verify(t, d, x, vl, T, uu, workspace=ws)
+    assert sv.read_status(ws) == 0
+    o = H.oracle_verify(case, T=T)
+    P = H.compare(o, tok.cpu().numpy(), n.cpu().numpy(), greedy=T == 0)
+    H.assert_parity(P, prob=False)
+    assert (n.cpu().numpy() >= 0).all()
