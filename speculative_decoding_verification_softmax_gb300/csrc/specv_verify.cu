@@ -294,6 +294,15 @@ __device__ __forceinline__ float chunk_round_sums(const ReqState& rs, const char
     constexpr int HALF = kVecPerLane / 2;
     const uint4* vt = (const uint4*)(rt + (size_t)e0 * ES);
     const uint4* vd = (const uint4*)(rd + (size_t)e0 * ES);
+    // the second half's vectors are fetched while the first half is reduced
+#pragma unroll
+    for (int k = HALF; k < 2 * HALF; ++k) {
+        const int i = 32 * k + lane;
+        if (i < nvec) {
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(vt + i));
+            if (rs.mode == 1) asm volatile("prefetch.global.L1 [%0];" ::"l"(vd + i));
+        }
+    }
     float r[8];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -761,17 +770,34 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
         const float d = p.x - js.M_t;
         return p.y * pow2_f(d < -1000.f ? -1000 : (int)d);
     };
-    DF W = {0.f, 0.f};
-    for (int k = lane; k < L.nch; k += 32) W = df_add(W, DF{total_of(job, k), 0.f});
-    W = warp_sum_df(W);
+    // Chunk totals, each lane taking a block of consecutive chunks: the lane
+    // sums (in chunk order) and one inclusive two-float warp scan of them give
+    // the total W (lane 31) and the lane whose block the draw falls in; that
+    // lane walks its block from its exclusive prefix.
+    const int cpl = (L.nch + 31) / 32;
+    const int k0 = min(L.nch, lane * cpl), k1 = min(L.nch, k0 + cpl);
+    DF lsum, incl;
+    int lpos;  // this lane's last chunk with positive total, or -1
+    auto block_scan = [&]() {
+        lsum = DF{0.f, 0.f};
+        lpos = -1;
+#pragma unroll 4
+        for (int k = k0; k < k1; ++k) {
+            const float v = total_of(job, k);
+            lsum = df_add(lsum, DF{v, 0.f});
+            if (v > 0.f) lpos = k;
+        }
+        incl = warp_scan_df(lsum, lane);
+    };
+    block_scan();
+    DF W = {__shfl_sync(0xffffffffu, incl.hi, 31), __shfl_sync(0xffffffffu, incl.lo, 31)};
     if (!(W.hi > 0.f) && job.mode == 1) {
         // the residual summed to zero: draw from p of the same row instead
         job.mode = 2;
         rd = rt;
         if (lane == 0) atomicOr(&hdr[kHdrEvents], 1);
-        W = DF{0.f, 0.f};
-        for (int k = lane; k < L.nch; k += 32) W = df_add(W, DF{total_of(job, k), 0.f});
-        W = warp_sum_df(W);
+        block_scan();
+        W = DF{__shfl_sync(0xffffffffu, incl.hi, 31), __shfl_sync(0xffffffffu, incl.lo, 31)};
     }
     // target = u * W as a two-float number
     DF target;
@@ -780,24 +806,36 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
         const float pe = fmaf(job.u, W.hi, -p);
         target = df_add(DF{p, 0.f}, DF{pe + job.u * W.lo, 0.f});
     }
-    // level 1: chunk totals
-    int cstar = -1, last_pos = -1;
-    DF before = {0.f, 0.f}, run = {0.f, 0.f};
-    for (int base = 0; base < L.nch && cstar < 0; base += 32) {
-        const int k = base + lane;
-        const float v = k < L.nch ? total_of(job, k) : 0.f;
-        DF excl;
-        const int l = scan_find(DF{v, 0.f}, df_add(target, DF{-run.hi, -run.lo}), lane, excl);
-        const unsigned pos = __ballot_sync(0xffffffffu, v > 0.f);
-        if (pos) last_pos = base + 31 - __clz(pos);
-        if (l >= 0) {
-            cstar = base + l;
-            before = df_add(run, excl);
-        } else {
-            DF blk = warp_sum_df(DF{v, 0.f});
-            run = df_add(run, blk);
+    auto exceeds = [](DF x, DF t) { return x.hi > t.hi || (x.hi == t.hi && x.lo > t.lo); };
+    int cstar = -1;
+    DF before = {0.f, 0.f};
+    const unsigned hit = __ballot_sync(0xffffffffu, exceeds(incl, target));
+    if (hit) {
+        const int l = __ffs(hit) - 1;
+        DF excl = {__shfl_up_sync(0xffffffffu, incl.hi, 1), __shfl_up_sync(0xffffffffu, incl.lo, 1)};
+        if (lane == 0) excl = DF{0.f, 0.f};
+        if (lane == l) {
+            // the first chunk whose running prefix exceeds the target; if
+            // rounding of the walk leaves none, the block's last chunk
+            DF run = excl, prev = excl;
+            for (int k = k0; k < k1; ++k) {
+                prev = run;
+                run = df_add(run, DF{total_of(job, k), 0.f});
+                if (exceeds(run, target)) {
+                    cstar = k;
+                    break;
+                }
+            }
+            if (cstar < 0) cstar = k1 - 1;
+            before = prev;
         }
+        cstar = __shfl_sync(0xffffffffu, cstar, l);
+        before.hi = __shfl_sync(0xffffffffu, before.hi, l);
+        before.lo = __shfl_sync(0xffffffffu, before.lo, l);
     }
+    int last_pos = lpos;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) last_pos = max(last_pos, __shfl_xor_sync(0xffffffffu, last_pos, o));
     int tok;
     if (cstar < 0) {
         // rounding left no chunk: the last element with positive weight of the
