@@ -54,16 +54,27 @@ __device__ __forceinline__ bool in01(float u) { return u >= 0.0f && u < 1.0f; }
 // for an invalid row.
 template <bool GREEDY>
 __device__ __forceinline__ bool merge_row(const float2* part, int nch, int lane, float& M, DF& S, int& arg) {
+    // the first 4 * 32 partials are loaded at once (constant register slots);
+    // longer rows continue in a loop
+    constexpr int K = 4;
+    float2 keep[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const int c = lane + 32 * k;
+        keep[k] = c < nch ? part[c] : make_float2(-INFINITY, GREEDY ? __int_as_float(0x7fffffff) : 0.f);
+    }
     if (GREEDY) {
         float best = -INFINITY;
         int ix = 0x7fffffff;
         bool bad = false;
-        for (int c = lane; c < nch; c += 32) {
-            const float2 p = part[c];
+        auto take = [&](float2 p) {
             const int i = __float_as_int(p.y);
             if (p.x != p.x) bad = true;
             else if (p.x > best || (p.x == best && i < ix)) { best = p.x; ix = i; }
-        }
+        };
+#pragma unroll
+        for (int k = 0; k < K; ++k) take(keep[k]);
+        for (int c = lane + 32 * K; c < nch; c += 32) take(part[c]);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             const float ob = __shfl_xor_sync(0xffffffffu, best, o);
@@ -78,28 +89,25 @@ __device__ __forceinline__ bool merge_row(const float2* part, int nch, int lane,
         return !bad && fabsf(best) <= 3.402823466e38f;
     }
     float m = -INFINITY;
-    float2 keep[4];
-    int nk = 0;
-    for (int c = lane; c < nch; c += 32) {
-        const float2 p = part[c];
-        if (nk < 4) keep[nk++] = p;
-        m = fmax_nan(m, p.x);
-    }
+#pragma unroll
+    for (int k = 0; k < K; ++k) m = fmax_nan(m, keep[k].x);
+    for (int c = lane + 32 * K; c < nch; c += 32) m = fmax_nan(m, part[c].x);
     m = warp_max_nan(m);
     M = m;
     arg = 0;
     if (m != m || m == -INFINITY) return false;
     DF acc = {0.f, 0.f};
-    int k = 0;
-    for (int c = lane; c < nch; c += 32, ++k) {
-        const float2 p = k < 4 ? keep[k] : part[c];
+    auto add = [&](float2 p) {
         if (p.x != -INFINITY) {
             // both scales are integer-valued: the rescale is an exact power of two
             const float d = p.x - m;
             const float v = p.y * pow2_f(d < -1000.f ? -1000 : (int)d);
             acc = df_add(acc, DF{v, 0.f});
         }
-    }
+    };
+#pragma unroll
+    for (int k = 0; k < K; ++k) add(keep[k]);
+    for (int c = lane + 32 * K; c < nch; c += 32) add(part[c]);
     S = warp_sum_df(acc);
     return S.hi > 0.f && S.hi <= 3.0e38f;
 }
@@ -623,6 +631,7 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
             const int j = lane;
             bool acc = true;
             float px = __int_as_float(0x7fc00000), qx = px;
+            DF rho_j = {0.f, 0.f};  // S_t / S_d of position j, in case the draw is its residual
             if (j < ell) {
                 if (GREEDY) {
                     acc = x == s_row[j].arg;
@@ -630,6 +639,7 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
                     px = div_df(scaled_exp(s_zt[j], a.c_hi, a.c_lo, s_row[j].M), s_row[j].S);
                     qx = div_df(scaled_exp(s_zd[j], a.c_hi, a.c_lo, s_row[ell + 1 + j].M), s_row[ell + 1 + j].S);
                     acc = __fmul_rn(uj, qx) < px;
+                    rho_j = df_div(s_row[j].S, s_row[ell + 1 + j].S);
                 }
             }
             const unsigned rej = __ballot_sync(0xffffffffu, !acc);
@@ -640,13 +650,14 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
             o.M_t = s_row[n].M;
             o.S_hi = St.hi;
             o.S_lo = St.lo;
+            const float rho_hi = __shfl_sync(0xffffffffu, rho_j.hi, n & 31);
+            const float rho_lo = __shfl_sync(0xffffffffu, rho_j.lo, n & 31);
             if (!GREEDY && n < ell) {
                 o.mode = 1;
                 o.g_d = T1 + b * a.gamma + n;
                 o.M_d = s_row[ell + 1 + n].M;
-                const DF rho = df_div(St, s_row[ell + 1 + n].S);
-                o.rho_hi = rho.hi;
-                o.rho_lo = rho.lo;
+                o.rho_hi = rho_hi;
+                o.rho_lo = rho_lo;
                 o.u = ug;
             } else if (!GREEDY) {
                 o.mode = 2;
