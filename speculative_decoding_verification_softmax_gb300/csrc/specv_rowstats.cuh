@@ -44,6 +44,8 @@ constexpr size_t kBarBytes = (size_t)kStatsWarps * kStages * 8;
 constexpr size_t kDescBytes = (size_t)kStatsWarps * kStages * sizeof(StageDesc);
 constexpr size_t kPrefixBytes = (SPEC_MAX_BATCH + 1) * 4;
 constexpr size_t kStatsSmem = kRingBytes + kBarBytes + kDescBytes + kPrefixBytes + kTableRows * 4 + 128;
+// the packed layout keeps each compact row's packed row index beside the table
+constexpr size_t kStatsSmemPacked = kStatsSmem + kTableRows * 4;
 constexpr int kVecPerLane = kChunkBytes / 16 / 32;  // 16-byte vectors per lane in one chunk
 
 struct StatsArgs {
@@ -123,15 +125,23 @@ __device__ void block_row_prefix(const int32_t* verify_len, const RowMap& rm, in
     __syncthreads();
 }
 
-// table[r] = global row id of compact row r (when the total fits): one warp
-// per request writes its rows.  No barrier inside.
-template <bool GREEDY>
-__device__ void block_row_table(const int* prefix, int B, int gamma, int* table) {
+// table[r] = global row id of compact row r (when the total fits), and for
+// the packed layout ptable[r] = its row in the packed target or draft array:
+// one warp per request writes its rows.  No barrier inside.
+template <bool GREEDY, bool PACKED>
+__device__ void block_row_table(const int* prefix, int B, int gamma, const RowMap& rm, int* table, int* ptable) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int T1 = B * (gamma + 1);
     for (int b = warp; b < B; b += kStatsWarps) {
         const int p0 = prefix[b], cnt = prefix[b + 1] - p0;
-        for (int k = lane; k < cnt; k += 32) table[p0 + k] = row_id<GREEDY>(b, k, cnt, gamma, T1);
+        if (cnt == 0) continue;
+        const int ell = GREEDY ? cnt - 1 : (cnt - 1) >> 1;
+        const int t0 = PACKED ? rm.trow[b] : 0;
+        const int d0 = (PACKED && !GREEDY && ell > 0) ? rm.drow[b] : 0;
+        for (int k = lane; k < cnt; k += 32) {
+            table[p0 + k] = row_id<GREEDY>(b, k, cnt, gamma, T1);
+            if (PACKED) ptable[p0 + k] = k <= ell ? t0 + k : d0 + (k - ell - 1);
+        }
     }
 }
 
@@ -282,6 +292,7 @@ __global__ void __launch_bounds__(kStatsThreads, 1) k_row_stats(StatsArgs a, Lay
     StageDesc* desc = (StageDesc*)(smem + kRingBytes + kBarBytes) + warp * kStages;
     int* prefix = (int*)(smem + kRingBytes + kBarBytes + kDescBytes);
     int* table = prefix + (SPEC_MAX_BATCH + 1);
+    int* ptable = table + kTableRows;  // packed layout only (in its larger allocation)
     int* hdr = (int*)(a.ws + L.hdr);
     float2* partial = (float2*)(a.ws + L.partial);
     __shared__ int s_exited, s_failed;  // warps done / any wait expired (this CTA)
@@ -337,8 +348,9 @@ __global__ void __launch_bounds__(kStatsThreads, 1) k_row_stats(StatsArgs a, Lay
         const int cnt = prefix[k.b + 1] - prefix[k.b];
         return row_id<GREEDY>(k.b, k.r - prefix[k.b], cnt, a.gamma, T1);
     };
-    auto row_ptr = [&](int g) -> const char* {
+    auto row_ptr = [&](const Cursor& k, int g) -> const char* {
         if constexpr (!PACKED) return g < T1 ? a.target + (size_t)g * a.V * ES : a.draft + (size_t)(g - T1) * a.V * ES;
+        if (table_ready) return (g < T1 ? a.target : a.draft) + (size_t)ptable[k.r] * a.V * ES;
         if (g < T1) {
             const int b = g / (a.gamma + 1);
             return a.target + target_row(a.rm, b, g - b * (a.gamma + 1), a.gamma + 1) * a.V * ES;
@@ -370,7 +382,7 @@ __global__ void __launch_bounds__(kStatsThreads, 1) k_row_stats(StatsArgs a, Lay
     // Issue the copy of the item under the issue cursor into stage s.
     auto issue = [&](int s) {
         const int g = row_of(ic);
-        const char* rowp = row_ptr(g);
+        const char* rowp = row_ptr(ic, g);
         const int e0 = ic.c * L.CH, e1 = min(a.V, e0 + L.CH);
         bool copy;
         const char* src;
@@ -405,7 +417,7 @@ __global__ void __launch_bounds__(kStatsThreads, 1) k_row_stats(StatsArgs a, Lay
     for (int s = 0; s < kStages && issued < count; ++s) issue(s);
     // the row table is built while those copies are in flight
     if (use_table) {
-        block_row_table<GREEDY>(prefix, a.B, a.gamma, table);
+        block_row_table<GREEDY, PACKED>(prefix, a.B, a.gamma, a.rm, table, ptable);
         __syncthreads();
         table_ready = true;
     }

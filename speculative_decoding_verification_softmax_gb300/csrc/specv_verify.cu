@@ -991,9 +991,9 @@ int device_info(int& sms) {
             (const void*)k_row_stats<4, false, false, true>,  (const void*)k_row_stats<4, true, false, true>,
             (const void*)k_row_stats<2, false, true, true>,   (const void*)k_row_stats<2, true, true, true>,
             (const void*)k_row_stats<4, false, true, true>,   (const void*)k_row_stats<4, true, true, true>};
-        for (const void* f : fns)
-            if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStatsSmem) !=
-                cudaSuccess)
+        for (int i = 0; i < 16; ++i)  // entries 8..15: the packed layout's instantiations
+            if (cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)(i < 8 ? kStatsSmem : kStatsSmemPacked)) != cudaSuccess)
                 return SPEC_ERR_CUDA;
         d.attrs_set = true;
     }
@@ -1028,7 +1028,7 @@ int launch_chain(const StatsArgs& sa, const FinishArgs& fa, const Layout& L, int
         cudaLaunchConfig_t kc = {};
         kc.gridDim = dim3((unsigned)grid);
         kc.blockDim = dim3(kStatsThreads);
-        kc.dynamicSmemBytes = kStatsSmem;
+        kc.dynamicSmemBytes = packed ? kStatsSmemPacked : kStatsSmem;
         kc.stream = st;
         kc.attrs = pa;
         kc.numAttrs = 1;
