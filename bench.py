@@ -752,21 +752,42 @@ def run_ours(args):
 
 
 def run_profile_case(args):
-    """A small case for ncu captures: B requests of the same workload (inputs
-    still larger than L2), a few spec_verify calls, nothing else."""
+    """A small case for ncu captures: B requests of one workload (inputs still
+    larger than L2), a few verification calls, nothing else.  --profile-packed
+    verifies the block-diffusion rows at D-cut lengths packed as [K, V]."""
+    import math
     import torch
     import specsynth
     import speculative_decoding_verification_softmax_gb300 as sv
     sv.build()
-    case = specsynth.make_verify_case(WORKLOAD, B=args.profile_batch)
+    name = args.profile_workload
+    case = specsynth.make_verify_case(name, B=args.profile_batch)
+    B, gamma, V = case.B, case.gamma, case.V
     t, d, x, vl, u = specsynth.to_device(case)
-    ws = sv.alloc_verify_workspace(case.B, case.gamma, case.V, sv.BF16)
+    dt = sv.BF16 if case.dtype == "bf16" else sv.F32
+    ws = sv.alloc_verify_workspace(B, gamma, V, dt)
+    uu = u if case.T != 0 else None
+    if args.profile_packed:
+        conf = torch.from_numpy(specsynth.make_confidences(B, gamma)).cuda()
+        kt, kc = specsynth.COST_TABLES[COST_READING]
+        ratios = [0.25, 0.5, 0.75, 1.0]
+        costs = [float(np.interp(max(B, math.ceil(r * B * (gamma + 1))), kt, kc)) for r in ratios]
+        vl, _ = sv.schedule(conf, (ratios, costs), 0, sv.SCHED_DCUT)
+        tr, dr, tot = sv.pack_rows(vl, gamma)
+        vl_h = vl.cpu().numpy()
+        ti = np.concatenate([b * (gamma + 1) + np.arange(vl_h[b] + 1) for b in range(B)])
+        di = np.concatenate([b * gamma + np.arange(vl_h[b]) for b in range(B)])
+        tp = t.view(-1, V)[torch.from_numpy(ti).cuda()].contiguous()
+        dp = d.view(-1, V)[torch.from_numpy(di).cuda()].contiguous()
+        call = lambda: sv.verify_packed(tp, dp, tr, dr, x, vl, case.T, u, workspace=ws)
+    else:
+        call = lambda: sv.verify(t, d, x, vl, case.T, uu, workspace=ws)
     for _ in range(args.warmup + args.steps):
-        sv.verify(t, d, x, vl, case.T, u, workspace=ws)
+        call()
     torch.cuda.synchronize()
     st = sv.read_status(ws)
-    print(json.dumps({"profile_case": WORKLOAD, "B": case.B, "calls": args.warmup + args.steps,
-                      "status": st}))
+    print(json.dumps({"profile_case": name, "packed": bool(args.profile_packed), "B": B,
+                      "calls": args.warmup + args.steps, "status": st}))
     if st != 0:
         raise SystemExit(1)
 
@@ -798,6 +819,10 @@ def main(argv=None):
     ap.add_argument("--profile-case", action="store_true",
                     help="run only a small case for ncu (B=--profile-batch)")
     ap.add_argument("--profile-batch", type=int, default=24)
+    ap.add_argument("--profile-workload", default=WORKLOAD, choices=["block_diffusion", "greedy", "mtp_chat"],
+                    help="workload of --profile-case")
+    ap.add_argument("--profile-packed", action="store_true",
+                    help="--profile-case on D-cut lengths with packed logits")
     ap.add_argument("--profile-sched", action="store_true",
                     help="run only the scheduler on the scheduled workload (for ncu)")
     ap.add_argument("--gpus", type=int, default=1)
