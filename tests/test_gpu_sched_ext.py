@@ -126,6 +126,7 @@ def test_sts_threshold(sv):
     confidence within 1e-12 of the threshold may fall either way: such
     requests are compared up to the first near-tie only."""
     rng = np.random.default_rng(51)
+    requests = excused = 0
     for trial in range(60):
         B = int(rng.integers(1, 2000))
         gamma = int(rng.integers(1, 33))
@@ -140,6 +141,10 @@ def test_sts_threshold(sv):
         clear = ref < first_near
         assert (g[clear] == ref[clear]).all()
         assert (np.minimum(g, first_near) == np.minimum(ref, first_near)).all()
+        requests += B
+        excused += int((~clear & (g != ref)).sum())
+    print(f"\n[sts threshold] requests={requests} excused near-ties={excused}")
+    assert excused <= 1e-3 * requests
 
 
 def test_sts_unit_temperatures_change_nothing(sv):
@@ -157,7 +162,7 @@ def test_sts_schedules(sv, mode):
     within 1e-9 (relative) of another allocation's objective are skipped,
     every other trial must agree exactly."""
     rng = np.random.default_rng({"exact": 61, "alg1": 62, "dcut": 63}[mode])
-    checked = 0
+    checked = excused = 0
     for trial in range(80):
         B = int(rng.integers(1, 200))
         gamma = int(rng.integers(1, 33))
@@ -190,8 +195,11 @@ def test_sts_schedules(sv, mode):
             assert g.sum() == ref["verify_len"].sum()
             prog = lambda v: sum(s[b, :v[b]].sum() for b in range(B))
             assert abs(prog(g) - prog(ref["verify_len"])) <= 1e-12 * prog(ref["verify_len"]), trial
+            excused += 1
         checked += 1
+    print(f"\n[sts {mode}] trials checked={checked} excused (equal count and progress)={excused}")
     assert checked > 40
+    assert excused <= max(1, 0.05 * checked)
 
 
 def test_sts_fit_from_verify_outcomes(sv):
