@@ -183,6 +183,10 @@ __global__ void __launch_bounds__(kSchedThreads, 1) k_schedule(SchedArgs a) {
     __shared__ int s_red_i[32];
     __shared__ int s_bad, s_npos, s_bestK, s_dcut_k;
 
+    // (no early trigger of the next kernel here: placing the verification's
+    // streaming CTAs on the other SMs while this cluster runs starts the 16
+    // CTAs that must wait for this cluster's SMs late, and the streaming
+    // pass's static split then ends late by as much)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int B = a.B, G = a.gamma, ml = a.min_len, per = G - ml, nc = a.nc, npad = a.npad;
     // With STS the fp64 powers are split over the cluster and the keys are
@@ -510,6 +514,7 @@ __global__ void __launch_bounds__(kSchedThreads, 1) k_schedule(SchedArgs a) {
 __global__ void __launch_bounds__(32) k_schedule_static(const float* conf, int G, double threshold, int max_len,
                                                         int min_len, int has_sts, SchedArgs sa, int32_t* out,
                                                         int* status) {
+    pdl_trigger();  // the next kernel may be placed now (it waits for these results)
     const int b = blockIdx.x, lane = threadIdx.x;
     bool bad = false, ok = true;
     if (conf && lane < G) {

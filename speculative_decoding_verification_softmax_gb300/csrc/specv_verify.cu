@@ -895,6 +895,7 @@ constexpr int kPackThreads = 1024;
 __global__ void __launch_bounds__(kPackThreads) k_pack_rows(const int32_t* verify_len, int B, int gamma,
                                                             int32_t* trow, int32_t* drow, int32_t* totals) {
     __shared__ int s_t[32], s_d[32];
+    pdl_trigger();  // the verification that follows may be placed now (it waits for these results)
     constexpr int PER = (SPEC_MAX_BATCH + kPackThreads - 1) / kPackThreads;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int ct[PER], cd[PER], mt = 0, md = 0;
