@@ -827,18 +827,29 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
         if (lane == 0) excl = DF{0.f, 0.f};
         if (lane == l) {
             // the first chunk whose running prefix exceeds the target; if
-            // rounding of the walk leaves none, the block's last chunk
-            DF run = excl, prev = excl;
+            // rounding of the walk leaves none, the block's last chunk with
+            // positive weight (the draw's rule for a target at the very end)
+            DF run = excl;
+            int lastp = -1;
+            DF before_lastp = excl;
             for (int k = k0; k < k1; ++k) {
-                prev = run;
-                run = df_add(run, DF{total_of(job, k), 0.f});
-                if (exceeds(run, target)) {
+                const float v = total_of(job, k);
+                const DF next = df_add(run, DF{v, 0.f});
+                if (v > 0.f) {
+                    lastp = k;
+                    before_lastp = run;
+                }
+                if (exceeds(next, target)) {
                     cstar = k;
+                    before = run;
                     break;
                 }
+                run = next;
             }
-            if (cstar < 0) cstar = k1 - 1;
-            before = prev;
+            if (cstar < 0) {
+                cstar = lastp >= 0 ? lastp : k1 - 1;
+                before = lastp >= 0 ? before_lastp : run;
+            }
         }
         cstar = __shfl_sync(0xffffffffu, cstar, l);
         before.hi = __shfl_sync(0xffffffffu, before.hi, l);

@@ -269,3 +269,19 @@ def test_wrappers_reject_mismatched_inputs():
         fn(dict(t=t, d=d, x=x, vl=vl, u=u))   # the well-formed call still runs
     torch.cuda.synchronize()
 
+
+
+@pytest.mark.parametrize("u_draw", [0.0, float(np.nextafter(np.float32(1.0), np.float32(0.0)))])
+@pytest.mark.parametrize("name", ["mtp_chat", "block_diffusion"])
+def test_draws_at_the_ends_of_the_cdf(name, u_draw):
+    """Residual and bonus draws with u = 0 (the first bin with positive
+    weight: the CDF test is strict) and u = 1 - 2^-24 (the last bins, where
+    rounding of the prefix sums may leave no bin above u * W and the draw
+    takes the last bin with positive weight): parity with the oracle."""
+    kw = dict(B=16) if name == "block_diffusion" else {}
+    case = specsynth.make_verify_case(name, **kw)
+    case.uniforms[:, case.gamma:] = np.float32(u_draw)
+    g, o, P = _run(case)
+    _report(f"{name} u={u_draw:.8f}", P)
+    assert g["device_status"] == 0
+    H.assert_parity(P)
