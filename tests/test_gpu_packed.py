@@ -224,3 +224,28 @@ def test_packed_no_drafts(sv, name):
     pad = H.gpu_verify(case)
     assert g["device_status"] == 0
     assert (g["tokens"] == pad["tokens"]).all() and (g["accept_len"] == 0).all()
+
+
+@pytest.mark.parametrize("name", ["mtp_chat", "greedy"])
+def test_packed_beyond_the_row_table(sv, name):
+    """More compact rows than the streaming kernel's shared-memory row table
+    holds (4096): the rows and their packed positions then come from the
+    request prefix and the row index in global memory.  512 requests with
+    ragged lengths, small vocabulary; identical to the padded call and at
+    parity with the oracle."""
+    case = specsynth.make_verify_case(name, B=512, gamma=16, V=520, seed_logits=910, seed_noise=911,
+                                      seed_tokens=912, seed_uniforms=913)
+    vl = _ragged(case, 77, lo=8)
+    case.verify_len[:] = vl
+    rows = int(((vl + 1) if case.T == 0 else (2 * vl + 1)).sum())
+    assert rows > 4096
+    r = oracle.pack_rows(vl, case.gamma)
+    tp, dp = _pack(case, vl, r["target_row"], r["draft_row"], r["K_target"], r["K_draft"], 0)
+    g = _run_packed(sv, case, vl, tp, dp, r["target_row"], r["draft_row"])
+    pad = H.gpu_verify(case)
+    for k in ("tokens", "accept_len", "status"):
+        assert (g[k] == pad[k]).all(), k
+    o = H.oracle_verify(case)
+    P = H.compare(o, g["tokens"], g["accept_len"], g["px"], g["qx"], g["mass"], g["status"], greedy=case.T == 0)
+    assert g["device_status"] == 0
+    H.assert_parity(P)
