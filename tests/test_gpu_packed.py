@@ -249,3 +249,36 @@ def test_packed_beyond_the_row_table(sv, name):
     P = H.compare(o, g["tokens"], g["accept_len"], g["px"], g["qx"], g["mass"], g["status"], greedy=case.T == 0)
     assert g["device_status"] == 0
     H.assert_parity(P)
+
+
+@pytest.mark.parametrize("name,gamma", [("mtp_chat", 2), ("greedy", 1)])
+def test_packed_row_map_read_from_global_memory(sv, name, gamma):
+    """1400 requests: more than a third of the request limit, so the streaming
+    kernel keeps no shared-memory copy of the row index and reads it from
+    global memory (with the row table at T = 0: at most 2800 rows; without it
+    at T > 0).  Identical to the padded call and at parity with the oracle;
+    then one request's target row moved past the end of the packed array is
+    marked and the others are unchanged."""
+    case = specsynth.make_verify_case(name, B=1400, gamma=gamma, V=520, seed_logits=920, seed_noise=921,
+                                      seed_tokens=922, seed_uniforms=923)
+    vl = _ragged(case, 78)
+    case.verify_len[:] = vl
+    r = oracle.pack_rows(vl, case.gamma)
+    tp, dp = _pack(case, vl, r["target_row"], r["draft_row"], r["K_target"], r["K_draft"], 0)
+    g = _run_packed(sv, case, vl, tp, dp, r["target_row"], r["draft_row"])
+    pad = H.gpu_verify(case)
+    for k in ("tokens", "accept_len", "status"):
+        assert (g[k] == pad[k]).all(), k
+    o = H.oracle_verify(case)
+    P = H.compare(o, g["tokens"], g["accept_len"], g["px"], g["qx"], g["mass"], g["status"], greedy=case.T == 0)
+    assert g["device_status"] == 0
+    H.assert_parity(P)
+
+    bad = int(np.flatnonzero(vl > 0)[-1])
+    trow = r["target_row"].copy()
+    trow[bad] = r["K_target"] - int(vl[bad])  # its last row one past the end
+    g2 = _run_packed(sv, case, vl, tp, dp, trow, r["draft_row"])
+    assert g2["status"][bad] == sv.ERR_ROW_INDEX and g2["accept_len"][bad] == -1
+    keep = np.arange(case.B) != bad
+    assert (g2["tokens"][keep] == pad["tokens"][keep]).all() and (g2["accept_len"][keep] == pad["accept_len"][keep]).all()
+    assert g2["device_status"] == sv.ERR_ROW_INDEX
