@@ -312,6 +312,33 @@ def graph_us_per_call(dev, stream, call, n_calls: int = 50, reps: int = 5) -> fl
     return e0.elapsed_time(e1) * 1e3 / (reps * n_calls)
 
 
+def head_start(n_calls: int, host_us_per_call: float = 100.0) -> None:
+    """Keep the GPU busy (a device-side sleep, launched before any event of
+    the loop that follows) while the host enqueues the next n_calls calls, so
+    that those calls run back to back and no host launch gap falls inside an
+    event bracket."""
+    import torch
+    sleep = getattr(torch.cuda, "_sleep", None)
+    if sleep is not None:
+        sleep(int(n_calls * host_us_per_call * 1e-6 * 2.2e9))  # cycles at up to 2.2 GHz
+
+
+def event_floor_ms(dev, stream, n: int = 50) -> float:
+    """Median time between the two events of a pair around an empty kernel,
+    launched back to back: what an event bracket adds to any kernel's
+    duration on this GPU (context for the event-bracketed kernel times)."""
+    import torch
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    torch.cuda.synchronize(dev)
+    head_start(n, 20.0)
+    for a, b in pairs:
+        a.record(stream)
+        torch.cuda._sleep(0)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    return float(np.median([a.elapsed_time(b) for a, b in pairs]))
+
+
 def row_stats_ms(sv, dev, stream, call, n: int) -> float:
     """Mean duration of the row-statistics kernel over n host-launched calls
     (call(i)), from an event pair recorded on the launching stream right
@@ -322,6 +349,7 @@ def row_stats_ms(sv, dev, stream, call, n: int) -> float:
         a.record(stream)
         b.record(stream)
     torch.cuda.synchronize(dev)
+    head_start(n)
     for i, (a, b) in enumerate(pairs):
         sv.profile_events(a, b)
         call(i)
@@ -330,12 +358,13 @@ def row_stats_ms(sv, dev, stream, call, n: int) -> float:
     return sum(a.elapsed_time(b) for a, b in pairs) / n
 
 
-def roofline_entry(alg_bytes: float, ms: float, launches: int) -> dict:
+def roofline_entry(alg_bytes: float, ms: float, launches: int, floor_ms: float | None = None) -> dict:
     peak, peak_kind = measured_peak_gbs()
     achieved = alg_bytes / (ms / 1e3) / 1e9
     return {"kernel": "k_row_stats", "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak, "algorithmic_bytes_per_launch": alg_bytes, "avg_launch_ms": ms,
-            "launches_timed": launches, "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})"}
+            "launches_timed": launches, "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
+            "event_pair_floor_ms": floor_ms}
 
 
 def time_other_workloads(sv, specsynth, dev, stream, rank: int):
@@ -452,6 +481,7 @@ def time_packed_step(sv, specsynth, case, t, d, x, u, dev, stream, rank: int, st
     rows = int(vl_h.sum())
     logit_bytes = (Kt + Kd) * V * 2
     k1 = row_stats_ms(sv, dev, stream, step, max(3, min(steps, 200)))
+    floor_ms = event_floor_ms(dev, stream)
     if sv.read_status(ws) != 0 or sv.read_status(sws) != 0:
         raise RuntimeError("device status on the packed step")
     return {"workload": "D-cut budget (ratios 0.25..1, costs = the round-cost table at K_rho), dense packing, "
@@ -462,7 +492,7 @@ def time_packed_step(sv, specsynth, case, t, d, x, u, dev, stream, rank: int, st
                       f"({n_sets * logit_bytes / 1e6:.0f} MB, L2 {l2 / 1e6:.0f} MB)",
             "host_launched_ms_per_step": host_ms, "host_launched_steps": steps,
             "kernel_launches_per_step": 2 + sv.kernel_count(B, case.T),
-            "roofline": roofline_entry(logit_bytes, k1, max(3, min(steps, 200)))}
+            "roofline": roofline_entry(logit_bytes, k1, max(3, min(steps, 200)), floor_ms)}
 
 
 def run_ours(args):
@@ -530,6 +560,7 @@ def run_ours(args):
         a.record(stream)
         b.record(stream)
     torch.cuda.synchronize(dev)
+    head_start(min(args.steps, 1000))
     for a, b in pairs:
         sv.profile_events(a, b)
         step()
@@ -537,6 +568,7 @@ def run_ours(args):
     sv.profile_events(None, None)
     k1_ms = sum(a.elapsed_time(b) for a, b in pairs) / len(pairs)
     k1_list = sorted(a.elapsed_time(b) for a, b in pairs)
+    floor_ms = event_floor_ms(dev, stream)  # reported beside the event-bracketed kernel times
 
     # timed region 3: each call bracketed by its own event pair (at call
     # boundaries, where nothing overlaps) for the latency distribution
@@ -595,7 +627,8 @@ def run_ours(args):
     rv_ms = graph_us_per_call(dev, stream, ragged_verify) / 1e3
     n_rag = out_n.cpu().numpy()
     ragged_resid = int(((n_rag < vl_h) * 2 + (n_rag >= vl_h)).sum()) * V * 2
-    rk1 = row_stats_ms(sv, dev, stream, sched_step, max(3, min(args.steps, 200)))
+    # the streaming kernel of the verification alone at the scheduled lengths
+    rk1 = row_stats_ms(sv, dev, stream, ragged_verify, max(3, min(args.steps, 200)))
     del ssets
     if sv.read_status(ws) != 0 or sv.read_status(ws_s) != 0:
         raise RuntimeError("device status on the scheduled workload")
@@ -613,7 +646,8 @@ def run_ours(args):
                                       / (rv_ms / 1e3) / 1e9 / measured_peak_gbs()[0],
                                       "timing": "50 calls in a CUDA graph, 5 replays; logits alternate "
                                                 "between two copies"},
-                      "roofline": roofline_entry(ragged_bytes, rk1, max(3, min(args.steps, 200)))}
+                      "roofline": dict(roofline_entry(ragged_bytes, rk1, max(3, min(args.steps, 200)), floor_ms),
+                                       calls="the verification alone at the scheduled lengths")}
     sched = time_schedulers(sv, dev, stream, rank)
     scheduled_step["scheduler_share"] = sched["modes"]["exact"]["us_per_call"] / 1e3 / s_ms
     packed_step = time_packed_step(sv, specsynth, case, t, d, x, u, dev, stream, rank, s_steps)
@@ -726,7 +760,8 @@ def run_ours(args):
                      "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": alg_bytes, "avg_launch_ms": k1_ms,
                      "launches_timed": args.steps,
-                     "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})"},
+                     "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
+                     "event_pair_floor_ms": floor_ms},
         "cpu_baseline": cpu_baseline(case, cores),
         "e2e": {"value": aggregate(e2e_ms, rows_per_step, world), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
