@@ -47,6 +47,22 @@ def test_parity_configs(name):
     H.assert_parity(P)
 
 
+@pytest.mark.parametrize("offset", [1000, 2000])
+@pytest.mark.parametrize("name", ["mtp_chat", "block_diffusion", "greedy"])
+def test_parity_configs_other_seeds(name, offset):
+    """The same workloads at full size on two more seed sets (every seed of
+    the recipe moved by the offset): other logits, drafts and uniforms, so
+    other rejection positions and draws."""
+    spec = specsynth.CONFIGS[name]
+    case = specsynth.make_verify_case(name, seed_logits=spec.seed_logits + offset, seed_noise=spec.seed_noise + offset,
+                                      seed_tokens=spec.seed_tokens + offset,
+                                      seed_uniforms=spec.seed_uniforms + offset, seed_boost=spec.seed_boost + offset)
+    g, o, P = _run(case)
+    _report(f"{name}+{offset}", P)
+    assert g["device_status"] == 0
+    H.assert_parity(P)
+
+
 def test_parity_scheduled_ragged():
     """Schedule on the GPU (lengths stay on the device), then verify the
     block-diffusion logits at those ragged lengths."""
