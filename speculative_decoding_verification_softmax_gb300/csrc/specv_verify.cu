@@ -594,7 +594,11 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
         if (!ok) rs.S = DF{__int_as_float(0x7fc00000), 0.f};
         if (lane < cs) *cluster.map_shared_rank(&s_row[r], lane) = rs;  // to every CTA of the request
     }
-    cluster.sync();
+    // a one-CTA cluster needs only the CTA barrier for its own shared memory
+    if (cs == 1)
+        __syncthreads();
+    else
+        cluster.sync();
 
     // 3. accept decision (identical in every CTA)
     if (warp == 0) {
@@ -756,7 +760,10 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
         }
         if (!tot_smem) __threadfence();
     }
-    cluster.sync();
+    if (cs == 1)
+        __syncthreads();
+    else
+        cluster.sync();
     if (rank != 0 || warp != 0) return;
 
     // 5. the draw (rank 0, warp 0)
