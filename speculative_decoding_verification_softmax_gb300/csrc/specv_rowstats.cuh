@@ -62,26 +62,13 @@ struct StatsArgs {
 // Rows a request needs: target 0..ell and (T > 0) draft 0..ell-1; 0 when
 // verify_len is out of range or packed rows fall outside the packed arrays
 // (the finish kernel marks the request invalid).
-// Packed layout: t0 / d0 receive the request's first packed target / draft
-// row, loaded together with verify_len (one memory latency, not two).
 template <bool GREEDY, bool PACKED>
-__device__ __forceinline__ int rows_of(const int32_t* verify_len, const RowMap& rm, int b, int gamma, int& t0,
-                                       int& d0) {
+__device__ __forceinline__ int rows_of(const int32_t* verify_len, const RowMap& rm, int b, int gamma) {
     const int ell = verify_len ? verify_len[b] : gamma;
-    t0 = PACKED ? rm.trow[b] : 0;
-    d0 = (PACKED && !GREEDY && rm.drow) ? rm.drow[b] : 0;
     if (ell < 0 || ell > gamma) return 0;
-    if (PACKED) {
-        const bool t_ok = t0 >= 0 && t0 <= rm.Kt - ell - 1;
-        const bool d_ok = GREEDY || ell == 0 || (d0 >= 0 && d0 <= rm.Kd - ell);
-        if (!(t_ok && d_ok)) return 0;
-    }
+    if (PACKED && !rows_in_range(rm, b, ell, !GREEDY)) return 0;
     return GREEDY ? ell + 1 : 2 * ell + 1;
 }
-
-// Shared-memory copy of the packed row map, kept in the prefix array's unused
-// slots (prefix[B+1 .. 3B]) when the batch leaves room for it.
-__host__ __device__ constexpr bool row_map_stash_fits(int B) { return 3 * B <= SPEC_MAX_BATCH; }
 
 // Global row id of row k of request b (which needs cnt rows).
 template <bool GREEDY>
@@ -91,9 +78,7 @@ __device__ __forceinline__ int row_id(int b, int k, int cnt, int gamma, int T1) 
 }
 
 // prefix[b] = rows of requests < b, prefix[B] = total.  Whole CTA; ends
-// with a barrier, so every thread sees the prefix.  Packed layout, when
-// row_map_stash_fits(B): also prefix[B + 1 + b] = trow[b] and
-// prefix[2B + 1 + b] = drow[b].
+// with a barrier, so every thread sees the prefix.
 template <bool GREEDY, bool PACKED>
 __device__ void block_row_prefix(const int32_t* verify_len, const RowMap& rm, int B, int gamma, int* prefix) {
     __shared__ int s_w[32];
@@ -102,16 +87,10 @@ __device__ void block_row_prefix(const int32_t* verify_len, const RowMap& rm, in
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int cnt[PER];
     int mine = 0;
-    const bool stash = PACKED && row_map_stash_fits(B);
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
         const int b = tid * PER + i;
-        int t0 = 0, d0 = 0;
-        cnt[i] = b < B ? rows_of<GREEDY, PACKED>(verify_len, rm, b, gamma, t0, d0) : 0;
-        if (stash && b < B) {
-            prefix[B + 1 + b] = t0;
-            prefix[2 * B + 1 + b] = d0;
-        }
+        cnt[i] = b < B ? rows_of<GREEDY, PACKED>(verify_len, rm, b, gamma) : 0;
         mine += cnt[i];
     }
     int incl = mine;
@@ -147,20 +126,18 @@ __device__ void block_row_prefix(const int32_t* verify_len, const RowMap& rm, in
 }
 
 // table[r] = global row id of compact row r (when the total fits), and for
-// the packed layout ptable[r] = its row in the packed target or draft array
-// (from the shared-memory row map when block_row_prefix kept one): one warp
-// per request writes its rows.  No barrier inside.
+// the packed layout ptable[r] = its row in the packed target or draft array:
+// one warp per request writes its rows.  No barrier inside.
 template <bool GREEDY, bool PACKED>
 __device__ void block_row_table(const int* prefix, int B, int gamma, const RowMap& rm, int* table, int* ptable) {
-    const bool stash = PACKED && row_map_stash_fits(B);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int T1 = B * (gamma + 1);
     for (int b = warp; b < B; b += kStatsWarps) {
         const int p0 = prefix[b], cnt = prefix[b + 1] - p0;
         if (cnt == 0) continue;
         const int ell = GREEDY ? cnt - 1 : (cnt - 1) >> 1;
-        const int t0 = PACKED ? (stash ? prefix[B + 1 + b] : rm.trow[b]) : 0;
-        const int d0 = (PACKED && !GREEDY && ell > 0) ? (stash ? prefix[2 * B + 1 + b] : rm.drow[b]) : 0;
+        const int t0 = PACKED ? rm.trow[b] : 0;
+        const int d0 = (PACKED && !GREEDY && ell > 0) ? rm.drow[b] : 0;
         for (int k = lane; k < cnt; k += 32) {
             table[p0 + k] = row_id<GREEDY>(b, k, cnt, gamma, T1);
             if (PACKED) ptable[p0 + k] = k <= ell ? t0 + k : d0 + (k - ell - 1);
@@ -374,15 +351,12 @@ __global__ void __launch_bounds__(kStatsThreads, 1) k_row_stats(StatsArgs a, Lay
     auto row_ptr = [&](const Cursor& k, int g) -> const char* {
         if constexpr (!PACKED) return g < T1 ? a.target + (size_t)g * a.V * ES : a.draft + (size_t)(g - T1) * a.V * ES;
         if (table_ready) return (g < T1 ? a.target : a.draft) + (size_t)ptable[k.r] * a.V * ES;
-        const bool stash = row_map_stash_fits(a.B);
         if (g < T1) {
-            const int b = g / (a.gamma + 1), j = g - b * (a.gamma + 1);
-            const size_t row = stash ? (size_t)(prefix[a.B + 1 + b] + j) : target_row(a.rm, b, j, a.gamma + 1);
-            return a.target + row * a.V * ES;
+            const int b = g / (a.gamma + 1);
+            return a.target + target_row(a.rm, b, g - b * (a.gamma + 1), a.gamma + 1) * a.V * ES;
         }
-        const int gd = g - T1, b = gd / a.gamma, j = gd - b * a.gamma;
-        const size_t row = stash ? (size_t)(prefix[2 * a.B + 1 + b] + j) : draft_row(a.rm, b, j, a.gamma);
-        return a.draft + row * a.V * ES;
+        const int gd = g - T1, b = gd / a.gamma;
+        return a.draft + draft_row(a.rm, b, gd - b * a.gamma, a.gamma) * a.V * ES;
     };
 
     // Every warp ends here: the last warp of the CTA to leave writes the CTA's

@@ -594,8 +594,9 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
         if (!ok) rs.S = DF{__int_as_float(0x7fc00000), 0.f};
         if (lane < cs) *cluster.map_shared_rank(&s_row[r], lane) = rs;  // to every CTA of the request
     }
-    // a one-CTA cluster needs only the CTA barrier for its own shared memory
-    if (cs == 1)
+    // a one-CTA cluster (at T = 0) needs only the CTA barrier for its own
+    // shared memory; the sampling instantiations keep the cluster barrier only
+    if (GREEDY && cs == 1)
         __syncthreads();
     else
         cluster.sync();
@@ -760,10 +761,7 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
         }
         if (!tot_smem) __threadfence();
     }
-    if (cs == 1)
-        __syncthreads();
-    else
-        cluster.sync();
+    cluster.sync();
     if (rank != 0 || warp != 0) return;
 
     // 5. the draw (rank 0, warp 0)

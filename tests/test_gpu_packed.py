@@ -253,12 +253,11 @@ def test_packed_beyond_the_row_table(sv, name):
 
 @pytest.mark.parametrize("name,gamma", [("mtp_chat", 2), ("greedy", 1)])
 def test_packed_row_map_read_from_global_memory(sv, name, gamma):
-    """1400 requests: more than a third of the request limit, so the streaming
-    kernel keeps no shared-memory copy of the row index and reads it from
-    global memory (with the row table at T = 0: at most 2800 rows; without it
-    at T > 0).  Identical to the padded call and at parity with the oracle;
-    then one request's target row moved past the end of the packed array is
-    marked and the others are unchanged."""
+    """1400 requests with ragged lengths on packed logits, with the row table
+    (T = 0: at most 2800 rows) and without it (T > 0: more than 4096 rows).
+    Identical to the padded call and at parity with the oracle; then one
+    request's target row moved past the end of the packed array is marked
+    and the others are unchanged."""
     case = specsynth.make_verify_case(name, B=1400, gamma=gamma, V=520, seed_logits=920, seed_noise=921,
                                       seed_tokens=922, seed_uniforms=923)
     vl = _ragged(case, 78)
