@@ -323,17 +323,20 @@ def head_start(n_calls: int, host_us_per_call: float = 100.0) -> None:
         sleep(int(n_calls * host_us_per_call * 1e-6 * 2.2e9))  # cycles at up to 2.2 GHz
 
 
-def event_floor_ms(dev, stream, n: int = 50) -> float:
+def event_floor_ms(dev, stream, n: int = 50) -> float | None:
     """Median time between the two events of a pair around an empty kernel,
     launched back to back: what an event bracket adds to any kernel's
     duration on this GPU (context for the event-bracketed kernel times)."""
     import torch
+    sleep = getattr(torch.cuda, "_sleep", None)  # a private PyTorch helper: report nothing without it
+    if sleep is None:
+        return None
     pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
     torch.cuda.synchronize(dev)
     head_start(n, 20.0)
     for a, b in pairs:
         a.record(stream)
-        torch.cuda._sleep(0)
+        sleep(0)
         b.record(stream)
     torch.cuda.synchronize(dev)
     return float(np.median([a.elapsed_time(b) for a, b in pairs]))
