@@ -764,12 +764,14 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
     cluster.sync();
     if (rank != 0 || warp != 0) return;
 
-    // 5. the draw (rank 0, warp 0)
-    if (SPLIT && job.mode == 1 && fsplit > 1) {
+    // 5. the draw (rank 0, warp 0); the request's state is read from shared
+    // memory here, so that the draw fits in the register budget without spills
+    ReqState& jd = s_job;
+    if (SPLIT && jd.mode == 1 && fsplit > 1) {
         // totals of the split chunks from their round sums, in round order
         for (int c = lane; c < L.nch; c += 32) {
             const int e0 = c * L.CH, e1 = min(a.V, e0 + L.CH);
-            if (chunk_vec<ES>(job, rt, rd, e0, e1)) {
+            if (chunk_vec<ES>(jd, rt, rd, e0, e1)) {
                 DF acc = {0.f, 0.f};
 #pragma unroll
                 for (int k = 0; k < 8; ++k) acc = df_add(acc, DF{s_rsum[c][k], 0.f});
@@ -778,7 +780,7 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
         }
         __syncwarp();
     }
-    const float2* tpart = partial + (size_t)job.g_t * L.nch;
+    const float2* tpart = partial + (size_t)jd.g_t * L.nch;
     auto total_of = [&](const ReqState& js, int c) -> float {
         if (js.mode == 1) return tot_smem ? s_ctot[c] : __ldcg(rchunk + c);
         const float2 p = tpart[c];
@@ -799,7 +801,7 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
         lpos = -1;
 #pragma unroll 4
         for (int k = k0; k < k1; ++k) {
-            const float v = total_of(job, k);
+            const float v = total_of(jd, k);
             lsum = df_add(lsum, DF{v, 0.f});
             if (v > 0.f) lpos = k;
         }
@@ -807,9 +809,9 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
     };
     block_scan();
     DF W = {__shfl_sync(0xffffffffu, incl.hi, 31), __shfl_sync(0xffffffffu, incl.lo, 31)};
-    if (!(W.hi > 0.f) && job.mode == 1) {
+    if (!(W.hi > 0.f) && jd.mode == 1) {
         // the residual summed to zero: draw from p of the same row instead
-        job.mode = 2;
+        jd.mode = 2;
         rd = rt;
         if (lane == 0) atomicOr(&hdr[kHdrEvents], 1);
         block_scan();
@@ -818,9 +820,9 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
     // target = u * W as a two-float number
     DF target;
     {
-        const float p = job.u * W.hi;
-        const float pe = fmaf(job.u, W.hi, -p);
-        target = df_add(DF{p, 0.f}, DF{pe + job.u * W.lo, 0.f});
+        const float p = jd.u * W.hi;
+        const float pe = fmaf(jd.u, W.hi, -p);
+        target = df_add(DF{p, 0.f}, DF{pe + jd.u * W.lo, 0.f});
     }
     auto exceeds = [](DF x, DF t) { return x.hi > t.hi || (x.hi == t.hi && x.lo > t.lo); };
     int cstar = -1;
@@ -838,7 +840,7 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
             int lastp = -1;
             DF before_lastp = excl;
             for (int k = k0; k < k1; ++k) {
-                const float v = total_of(job, k);
+                const float v = total_of(jd, k);
                 const DF next = df_add(run, DF{v, 0.f});
                 if (v > 0.f) {
                     lastp = k;
@@ -869,16 +871,16 @@ __global__ void __launch_bounds__(kFinThreads, 2) k_finish(FinishArgs a, Layout 
         // last chunk with positive weight
         cstar = last_pos >= 0 ? last_pos : L.nch - 1;
         const int e0 = cstar * L.CH, e1 = min(a.V, e0 + L.CH);
-        tok = chunk_pick<ES>(job, rt, rd, e0, e1, DF{INFINITY, 0.f}, lane, a.c_hi, a.c_lo);
+        tok = chunk_pick<ES>(jd, rt, rd, e0, e1, DF{INFINITY, 0.f}, lane, a.c_hi, a.c_lo);
         if (lane == 0) atomicOr(&hdr[kHdrEvents], 2);
     } else {
         const DF r = df_add(target, DF{-before.hi, -before.lo});
         const int e0 = cstar * L.CH, e1 = min(a.V, e0 + L.CH);
-        const float* rsum = (job.mode == 1 && round_smem) ? s_rsum[cstar] : nullptr;
-        tok = pick_in_chunk<ES>(job, rt, rd, e0, e1, r, rsum, lane, a.c_hi, a.c_lo);
+        const float* rsum = (jd.mode == 1 && round_smem) ? s_rsum[cstar] : nullptr;
+        tok = pick_in_chunk<ES>(jd, rt, rd, e0, e1, r, rsum, lane, a.c_hi, a.c_lo);
     }
     if (lane == 0) {
-        a.out_tokens[(size_t)b * G1 + job.n] = tok;
+        a.out_tokens[(size_t)b * G1 + jd.n] = tok;
         ((float2*)(a.ws + L.mass))[b] = make_float2(W.hi, W.lo);  // divided by S_t in k_copy_stats
     }
 }
